@@ -1,0 +1,320 @@
+"""CPU oracle for the FP8 rollout hot path -- TEST INFRASTRUCTURE ONLY.
+
+Plain, slow, obviously-correct restatement of what the library computes, used
+by the tests, by ``__graft_entry__.smoke()`` and by the benchmark's CPU
+baseline leg.  The product path (the CUDA library and its Python binding)
+never imports this package, and this package never imports the product.
+
+The arithmetic lives in ``fp8rl_oracle.cpp`` (plain C++, one IEEE operation
+per step, no fast-math, no FMA contraction); this module marshals numpy arrays
+into it and adds the few steps that are clearer in Python:
+
+* the exact resolution of the rare TIS inputs whose binary32 rounding the
+  float64 ``exp`` cannot decide (a 60-digit ``decimal`` exponential), and
+* the clip / mask of the TIS weights (numpy ``where``), and
+* the BF16 rounding of float64 GEMM outputs (a torch CPU cast).
+
+Each function names the passage of the FP8-RL pages it follows (summary page,
+sections 3.4.1-3.4.4; E4M3 per Micikevicius et al.).
+
+Parity status: every function here is pinned by tests/test_oracle_*.py except
+the two readings the pages leave open -- the KV scale formula (per-head
+amax/448, section 3.4.4 gives no formula) and the MoE routing-bias form of the
+synthetic inputs -- which are marked "parity unpinned" in the design doc.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from decimal import Decimal, localcontext
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+
+def threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i64, i32, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        L.orc_e4m3_decode.restype = ctypes.c_double
+        L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_encode.restype = ctypes.c_uint8
+        L.orc_e4m3_encode.argtypes = [f32]
+        L.orc_e4m3_encode_array.argtypes = [P, P, i64, ctypes.c_int]
+        L.orc_e4m3_decode_array.argtypes = [P, P, i64]
+        L.orc_quantize_values.argtypes = [P, P, P, i64, ctypes.c_int]
+        L.orc_quantize_weights_blockwise.argtypes = [P, i64, i64, i64, P, i64, P, ctypes.c_int]
+        L.orc_quantize_weight_blocks.argtypes = [P, i64, i64, i64, P, i64, P, P]
+        L.orc_quantize_act_groupwise.argtypes = [P, i64, i64, i64, P, P, ctypes.c_int]
+        L.orc_kv_calibrate.argtypes = [P, i64, ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
+        L.orc_kv_quantize.argtypes = [P, i64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int]
+        L.orc_gemm_w8a8_sampled.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P, i64, P, P,
+                                            ctypes.c_int]
+        L.orc_grouped_gemm_w8a8_sampled.argtypes = [P, P, P, P, P, i32, i64, i64, i64, P, i64,
+                                                    P, i64, P, P, ctypes.c_int]
+        L.orc_tis_exp.restype = i64
+        L.orc_tis_exp.argtypes = [P, P, i64, P, P, i64, ctypes.c_int]
+        _LIB = L
+    return _LIB
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    """BF16 data as its uint16 bit patterns (numpy has no bf16)."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            assert a.dtype == torch.bfloat16
+            return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.int16).numpy()
+                                        .view(np.uint16))
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.asarray(a)
+    assert a.dtype == np.uint16, "BF16 inputs are torch.bfloat16 tensors or uint16 bit arrays"
+    return np.ascontiguousarray(a)
+
+
+# ------------------------------------------------------------------ codec --
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each E4M3 code (float64; NaN for 0x7F / 0xFF)."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, dtype=np.float64)
+    lib().orc_e4m3_decode_array(_p(c), _p(out), c.size)
+    return out
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 code of each binary32 value: RNE, saturating at +-448, sign kept."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().orc_e4m3_encode_array(_p(x), _p(out), x.size, threads())
+    return out
+
+
+def quantize_values(x, s) -> np.ndarray:
+    """Code of binary32 x under binary32 scale s: E4M3(fl32(x / s)); s == 0 keeps +-0."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    s = np.ascontiguousarray(np.broadcast_to(np.asarray(s, dtype=np.float32), x.shape))
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().orc_quantize_values(_p(x), _p(s), _p(out), x.size, threads())
+    return out
+
+
+# ------------------------------------------------------------- quantizers --
+
+def quantize_weights_blockwise(w):
+    """128x128-block E4M3 quantization of a BF16 [n, k] matrix.
+
+    Returns (codes uint8 [n, k], scales float32 [ceil(n/128), ceil(k/128)]).
+    """
+    wb = _u16(w)
+    n, k = wb.shape
+    q = np.zeros((n, k), dtype=np.uint8)
+    s = np.zeros(((n + 127) // 128, (k + 127) // 128), dtype=np.float32)
+    lib().orc_quantize_weights_blockwise(_p(wb), n, k, k, _p(q), k, _p(s), threads())
+    return q, s
+
+
+def quantize_weight_blocks(w, block_ids):
+    """The same map on selected blocks only (row-major block ids).
+
+    Returns (codes uint8 [len(ids), 128, 128] zero-padded, scales float32 [len(ids)]).
+    """
+    wb = _u16(w)
+    n, k = wb.shape
+    ids = np.ascontiguousarray(np.asarray(block_ids, dtype=np.int64))
+    q = np.zeros((ids.size, 128, 128), dtype=np.uint8)
+    s = np.zeros(ids.size, dtype=np.float32)
+    lib().orc_quantize_weight_blocks(_p(wb), n, k, k, _p(ids), ids.size, _p(q), _p(s))
+    return q, s
+
+
+def quantize_act_groupwise(a):
+    """Per-token 1x128-group E4M3 quantization of a BF16 [m, k] matrix.
+
+    Returns (codes uint8 [m, k], scales float32 [ceil(k/128), m] group-major).
+    """
+    ab = _u16(a)
+    m, k = ab.shape
+    q = np.zeros((m, k), dtype=np.uint8)
+    s = np.zeros(((k + 127) // 128, m), dtype=np.float32)
+    lib().orc_quantize_act_groupwise(_p(ab), m, k, k, _p(q), _p(s), threads())
+    return q, s
+
+
+def kv_calibrate(x):
+    """Per-head scales fl32(amax/448) of a BF16 [rows, heads, head_dim] K or V tensor."""
+    xb = _u16(x)
+    rows, heads, hd = xb.shape
+    s = np.zeros(heads, dtype=np.float32)
+    lib().orc_kv_calibrate(_p(xb), rows, heads, hd, _p(s), threads())
+    return s
+
+
+def kv_quantize(x, scales):
+    """E4M3 codes of a BF16 [rows, heads, head_dim] tensor under per-head scales."""
+    xb = _u16(x)
+    rows, heads, hd = xb.shape
+    s = np.ascontiguousarray(np.asarray(scales, dtype=np.float32))
+    assert s.shape == (heads,)
+    q = np.zeros(xb.shape, dtype=np.uint8)
+    lib().orc_kv_quantize(_p(xb), rows, heads, hd, _p(s), _p(q), threads())
+    return q
+
+
+# ------------------------------------------------------------------ GEMMs --
+
+def _idx(v, n):
+    if v is None:
+        return np.arange(n, dtype=np.int64)
+    return np.ascontiguousarray(np.asarray(v, dtype=np.int64))
+
+
+def gemm_w8a8(qa, sa, qw, sw, rows=None, cols=None):
+    """float64 Y = A_deq W_deq^T on the selected rows/cols.
+
+    qa uint8 [M, K], sa float32 [K/128, M], qw uint8 [N, K],
+    sw float32 [ceil(N/128), K/128].  Returns (Y64 [nr, nc], absprod [nr, nc])
+    where absprod = |A_deq| |W_deq|^T (the per-element error scale).
+    """
+    qa = np.ascontiguousarray(qa, dtype=np.uint8)
+    qw = np.ascontiguousarray(qw, dtype=np.uint8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    M, K = qa.shape
+    N = qw.shape[0]
+    assert K % 128 == 0 and qw.shape[1] == K
+    assert sa.shape == (K // 128, M) and sw.shape == ((N + 127) // 128, K // 128)
+    r, c = _idx(rows, M), _idx(cols, N)
+    y = np.zeros((r.size, c.size), dtype=np.float64)
+    ab = np.zeros_like(y)
+    lib().orc_gemm_w8a8_sampled(_p(qa), _p(sa), _p(qw), _p(sw), M, N, K, _p(r), r.size,
+                                _p(c), c.size, _p(y), _p(ab), threads())
+    return y, ab
+
+
+def grouped_gemm_w8a8(qa, sa, qw, sw, offsets, rows=None, cols=None):
+    """Per-expert float64 GEMM: rows of segment e use expert e's weights.
+
+    qw uint8 [E, N, K], sw float32 [E, N/128, K/128], offsets int32 [E+1].
+    Rows outside all segments come back as NaN.
+    """
+    qa = np.ascontiguousarray(qa, dtype=np.uint8)
+    qw = np.ascontiguousarray(qw, dtype=np.uint8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    M, K = qa.shape
+    E, N, K2 = qw.shape
+    assert K2 == K and off.shape == (E + 1,)
+    r, c = _idx(rows, M), _idx(cols, N)
+    y = np.zeros((r.size, c.size), dtype=np.float64)
+    ab = np.zeros_like(y)
+    lib().orc_grouped_gemm_w8a8_sampled(_p(qa), _p(sa), _p(qw), _p(sw), _p(off), E, M, N, K,
+                                        _p(r), r.size, _p(c), c.size, _p(y), _p(ab),
+                                        threads())
+    return y, ab
+
+
+def bf16_round(y64) -> np.ndarray:
+    """BF16 (round-to-nearest-even) of fl32(Y64), returned widened to float32."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(y64, dtype=np.float64))
+    return t.to(torch.float32).to(torch.bfloat16).to(torch.float32).numpy()
+
+
+# --------------------------------------------------------------------- TIS --
+
+_F32_OVERFLOW = Decimal(2) ** 128   # RN overflows to inf at/after the midpoint below this
+
+
+def _dec(f32: np.float32) -> Decimal:
+    f = float(f32)
+    if np.isinf(f):
+        return _F32_OVERFLOW if f > 0 else -_F32_OVERFLOW
+    return Decimal(f)  # exact
+
+
+def exp_rn32_decimal(delta: np.float32) -> np.float32:
+    """Correctly rounded binary32 e^delta, decided with a 60-digit decimal exp.
+
+    e^delta is transcendental for delta != 0, so it never equals a rounding
+    boundary; 60 significant digits separate it from every boundary by a wide
+    margin.  Candidates are the float nearest the float64 estimate and its two
+    neighbours.
+    """
+    d = np.float32(delta)
+    if np.isnan(d):
+        return np.float32(np.nan)
+    with localcontext() as ctx:
+        ctx.prec = 60
+        v = Decimal(float(d)).exp()
+        with np.errstate(over="ignore"):
+            guess = np.float32(np.exp(np.float64(d)))
+        cands = {guess,
+                 np.nextafter(guess, np.float32(np.inf)),
+                 np.nextafter(guess, np.float32(-np.inf))}
+        cands = [c for c in cands if not (np.isinf(c) and c < 0) and not c < 0]
+        best = min(cands, key=lambda c: (abs(_dec(c) - v), int(np.float32(c).view(np.uint32)) & 1))
+    return np.float32(best)
+
+
+def tis_exp(logp_train, logp_rollout) -> np.ndarray:
+    """RN32(e^(fl32(lt - lr))) per token (the unclipped importance weight)."""
+    lt = np.ascontiguousarray(np.asarray(logp_train, dtype=np.float32))
+    lr = np.ascontiguousarray(np.asarray(logp_rollout, dtype=np.float32))
+    assert lt.shape == lr.shape
+    n = lt.size
+    e = np.empty(lt.shape, dtype=np.float32)
+    cap = max(1024, n // 4096)
+    hard = np.empty(cap, dtype=np.int64)
+    cnt = lib().orc_tis_exp(_p(lt), _p(lr), n, _p(e), _p(hard), cap, threads())
+    if cnt > cap:   # more boundary cases than expected: redo with room for all
+        hard = np.empty(cnt, dtype=np.int64)
+        cnt = lib().orc_tis_exp(_p(lt), _p(lr), n, _p(e), _p(hard), cnt, threads())
+    ef = e.reshape(-1)
+    ltf, lrf = lt.reshape(-1), lr.reshape(-1)
+    for i in hard[:cnt]:
+        ef[i] = exp_rn32_decimal(np.float32(ltf[i] - lrf[i]))
+    tis_exp.last_hard_count = int(cnt)
+    return e
+
+
+tis_exp.last_hard_count = 0
+
+
+def tis_weights(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_lo: float = 0.0):
+    """Token-level truncated importance weights.
+
+    Summary page, section 3.4.3: w = pi_theta / pi_fp8 = exp(logp_train -
+    logp_rollout), truncated at C = 2.  One-sided min(w, C) by default
+    (c_lo = 0); c_lo = 1/C gives the two-sided [1/C, C] clip the same section
+    also states.  Comparisons act on the rounded weight; NaN stays NaN; tokens
+    with mask == 0 get weight 0.
+    """
+    e = tis_exp(logp_train, logp_rollout)
+    hi, lo = np.float32(c_hi), np.float32(c_lo)
+    w = np.where(e > hi, hi, e)
+    if c_lo > 0:
+        w = np.where(e < lo, lo, w)
+    if mask is not None:
+        w = np.where(np.asarray(mask) == 0, np.float32(0), w)
+    return w.astype(np.float32)

@@ -1,0 +1,97 @@
+"""Pins of the oracle's truncated importance weights.
+
+* closed forms the pages' definition fixes (golden/tis_closed_forms.json);
+* correct rounding: the C float64 path plus decimal resolution agrees with a
+  pure-Python 60-digit decimal exponential on samples spanning the domain,
+  including every input the float64 path flagged as near a rounding boundary;
+* the weight is the ratio of probabilities: for probabilities given exactly
+  as binary32 numbers, w agrees with p_train / p_rollout to the accuracy the
+  logs allow;
+* clip semantics: NaN propagates, the mask zeroes, C and 1/C bound the result.
+"""
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle
+from fp8_precision_rollout_gb300 import workloads
+
+
+def test_closed_forms(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "tis_closed_forms.json")))
+    for c in g["cases"]:
+        lt = np.array([c["logp_train"]], dtype=np.float32)
+        lr = np.array([c["logp_rollout"]], dtype=np.float32)
+        w = oracle.tis_weights(lt, lr, c_hi=g["C"], c_lo=c["c_lo"])[0]
+        if "w_hex" in c:
+            assert hex(int(np.float32(w).view(np.uint32))) == hex(int(c["w_hex"], 16)), c["why"]
+        else:
+            assert w == np.float32(c["w"]), c["why"]
+
+
+def test_correct_rounding_against_decimal():
+    rng = np.random.default_rng(20)
+    parts = [
+        rng.uniform(-104, 0.7, 3000),
+        rng.normal(0, 0.05, 3000),
+        rng.normal(0, 1e-6, 1000),
+        np.ldexp(rng.uniform(0.5, 1, 1000), rng.integers(-40, -20, 1000)) * rng.choice([-1, 1], 1000),
+        rng.uniform(85, 90, 500),
+        rng.uniform(-104.5, -87, 500),
+    ]
+    d = np.concatenate(parts).astype(np.float32)
+    e = oracle.tis_exp(d, np.zeros_like(d))
+    for di, ei in zip(d, e):
+        assert np.float32(ei).view(np.uint32) == oracle.exp_rn32_decimal(di).view(np.uint32), di
+
+
+def test_flagged_boundary_cases_are_resolved_exactly():
+    # near 0, e^d sits close to binary32 midpoints (e.g. d = -2^-25 is 2^-51 above one)
+    d = np.array([-2.0 ** -25, 2.0 ** -24, -3 * 2.0 ** -25, 2.0 ** -30], dtype=np.float32)
+    e = oracle.tis_exp(d, np.zeros_like(d))
+    assert oracle.tis_exp.last_hard_count >= 1
+    for di, ei in zip(d, e):
+        assert ei == oracle.exp_rn32_decimal(di)
+    assert e[0] == np.float32(1.0)               # 1 - 2^-25 + 2^-51 is above the midpoint
+    # dense sweep: all floats in a window around 0 where many inputs are flagged
+    bits = np.arange(np.float32(2.0 ** -26).view(np.uint32), np.float32(2.0 ** -26).view(np.uint32) + 20000,
+                     dtype=np.uint32)
+    d = np.concatenate([bits.view(np.float32), -bits.view(np.float32)])
+    e = oracle.tis_exp(d, np.zeros_like(d))
+    sample = np.random.default_rng(21).choice(d.size, 400, replace=False)
+    for i in sample:
+        assert e[i] == oracle.exp_rn32_decimal(d[i])
+
+
+def test_weight_is_probability_ratio():
+    rng = np.random.default_rng(22)
+    p_roll = rng.uniform(1e-4, 1, 2000)
+    p_train = np.clip(p_roll * np.exp(rng.normal(0, 0.3, 2000)), 1e-6, 1)
+    lt = np.log(p_train).astype(np.float32)
+    lr = np.log(p_roll).astype(np.float32)
+    w = oracle.tis_weights(lt, lr, c_hi=1e30)
+    ratio = p_train / p_roll
+    # log-probs carry binary32 rounding (|log p| <= ~14): allow that in the exponent
+    tol = (np.abs(np.log(p_train)) + np.abs(np.log(p_roll))) * 2.0 ** -23 + 2.0 ** -22
+    assert (np.abs(w / ratio - 1) <= tol * 1.01).all()
+
+
+def test_clip_mask_nan():
+    lt, lr = workloads.tis_logprobs(4096, seed=0)
+    lt, lr = lt.numpy(), lr.numpy()
+    e = oracle.tis_exp(lt, lr)
+    w1 = oracle.tis_weights(lt, lr)
+    assert (w1 <= 2).all() and (w1 == np.minimum(e, np.float32(2))).all()
+    w2 = oracle.tis_weights(lt, lr, c_lo=0.5)
+    assert (w2 >= 0.5).all() and (w2 <= 2).all()
+    mask = (np.arange(4096) % 3 != 0).astype(np.uint8)
+    w3 = oracle.tis_weights(lt, lr, mask=mask)
+    assert (w3[mask == 0] == 0).all() and (w3[mask == 1] == w1[mask == 1]).all()
+    nan = np.array([np.nan, 0.0], dtype=np.float32)
+    w4 = oracle.tis_weights(nan, np.zeros(2, np.float32))
+    assert math.isnan(w4[0]) and w4[1] == 1.0
+    inf = np.array([np.inf, -np.inf], dtype=np.float32)
+    w5 = oracle.tis_weights(inf, np.zeros(2, np.float32))
+    assert w5[0] == 2.0 and w5[1] == 0.0
