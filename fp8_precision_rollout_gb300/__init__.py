@@ -5,4 +5,18 @@ The compute lives in a C-ABI CUDA library (``libfp8rl.so``, sources in
 ctypes layer with the same call names.  The library is loaded on the first
 call and a missing or unloadable library raises -- there is no fallback.
 """
-__all__ = ["workloads"]
+from .binding import (  # noqa: F401
+    FP8RL_KV_CALIBRATE,
+    FP8RL_KV_GIVEN,
+    Fp8rlError,
+    device_status,
+    gemm_w8a8_blockwise,
+    grouped_gemm_w8a8_blockwise,
+    last_error,
+    quantize_act_groupwise,
+    quantize_kv_fp8,
+    quantize_weights_blockwise,
+    quantize_weights_blockwise_multi,
+    tis_weights,
+    version,
+)

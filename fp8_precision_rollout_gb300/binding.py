@@ -1,0 +1,258 @@
+"""Thin ctypes binding of libfp8rl.so with the C ABI's call names.
+
+Argument marshalling only: every function checks dtypes/devices of the torch
+tensors it is given, allocates missing outputs with torch (device memory is
+torch's job here), and passes raw pointers plus the current CUDA stream to the
+library.  Every step of the computation runs in the library's kernels.  If the
+library is missing or fails to load, the first call raises -- there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp8rl.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "fp8rl.h")
+
+FP8RL_OK = 0
+FP8RL_KV_GIVEN = 0
+FP8RL_KV_CALIBRATE = 1
+_STATUS = {0: "FP8RL_OK", 1: "FP8RL_ERR_INVALID_ARG", 2: "FP8RL_ERR_ALIGNMENT",
+           3: "FP8RL_ERR_UNSUPPORTED_SHAPE", 4: "FP8RL_ERR_CUDA", 5: "FP8RL_ERR_TIMEOUT",
+           6: "FP8RL_ERR_UNSUPPORTED_DEVICE"}
+
+
+class Fp8rlError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (_STATUS.get(status, str(status)), message))
+        self.status = status
+
+
+class WDesc(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("q", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("n", ctypes.c_int64), ("k", ctypes.c_int64), ("ldw", ctypes.c_int64),
+                ("ldq", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load (once) and return the ctypes handle of libfp8rl.so."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError("libfp8rl.so not found at %s: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`" % p)
+    L = ctypes.CDLL(p)
+    P, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    sigs = {
+        "fp8rl_version": (i32, []),
+        "fp8rl_last_error": (ctypes.c_char_p, []),
+        "fp8rl_quantize_weights_blockwise": (ctypes.c_int, [P, i64, i64, i64, P, i64, P, P]),
+        "fp8rl_quantize_weights_blockwise_multi": (ctypes.c_int, [P, i32, P]),
+        "fp8rl_quantize_act_groupwise": (ctypes.c_int, [P, i64, i64, i64, P, P, P]),
+        "fp8rl_gemm_w8a8_blockwise": (ctypes.c_int, [P, P, P, P, i64, i64, i64, P, i64, P]),
+        "fp8rl_grouped_gemm_w8a8_blockwise": (ctypes.c_int, [P, P, P, P, P, i32, i64, i64, i64,
+                                                              P, P]),
+        "fp8rl_quantize_kv_fp8": (ctypes.c_int, [P, i64, i32, i32, i32, P, P, P]),
+        "fp8rl_tis_weights": (ctypes.c_int, [P, P, P, i64, f32, f32, P, P]),
+        "fp8rl_device_status": (ctypes.c_int, [i32, i32]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = L
+    return L
+
+
+def declared_symbols(header: str = HEADER) -> list:
+    """Names of the functions include/fp8rl.h declares."""
+    text = open(header).read()
+    return sorted(set(re.findall(r"\b(fp8rl_[a-z0-9_]+)\s*\(", text)))
+
+
+def last_error() -> str:
+    return load().fp8rl_last_error().decode()
+
+
+def version() -> int:
+    return int(load().fp8rl_version())
+
+
+def _check(status: int):
+    if status != FP8RL_OK:
+        raise Fp8rlError(status, last_error())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+def _rowmajor(t: torch.Tensor, name: str):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("%s must be a 2-D tensor with unit column stride" % name)
+    return t
+
+
+# -------------------------------------------------------------- quantizers --
+
+def quantize_weights_blockwise(w: torch.Tensor, q: Optional[torch.Tensor] = None,
+                               scales: Optional[torch.Tensor] = None, stream=None):
+    """128x128-block E4M3 quantization of a bf16 [n, k] weight -> (codes uint8, scales f32)."""
+    _rowmajor(_dev(w, torch.bfloat16, "w"), "w")
+    n, k = w.shape
+    if q is None:
+        q = torch.empty(n, k, dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((n + 127) // 128, (k + 127) // 128, dtype=torch.float32, device=w.device)
+    _rowmajor(_dev(q, torch.uint8, "q"), "q")
+    _dev(scales, torch.float32, "scales")
+    _check(load().fp8rl_quantize_weights_blockwise(w.data_ptr(), n, k, w.stride(0), q.data_ptr(),
+                                                   q.stride(0), scales.data_ptr(), _stream(stream)))
+    return q, scales
+
+
+def quantize_weights_blockwise_multi(ws: Sequence[torch.Tensor], qs=None, ss=None, stream=None):
+    """One launch over many weights (a whole model's per-step re-quantization)."""
+    ws = list(ws)
+    qs = list(qs) if qs is not None else [torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+                                          for w in ws]
+    ss = list(ss) if ss is not None else [
+        torch.empty((w.shape[0] + 127) // 128, (w.shape[1] + 127) // 128, dtype=torch.float32,
+                    device=w.device) for w in ws]
+    arr = (WDesc * max(1, len(ws)))()
+    for i, (w, q, s) in enumerate(zip(ws, qs, ss)):
+        _rowmajor(_dev(w, torch.bfloat16, "w[%d]" % i), "w")
+        _rowmajor(_dev(q, torch.uint8, "q[%d]" % i), "q")
+        _dev(s, torch.float32, "scales[%d]" % i)
+        arr[i] = WDesc(w.data_ptr(), q.data_ptr(), s.data_ptr(), w.shape[0], w.shape[1],
+                       w.stride(0), q.stride(0))
+    _check(load().fp8rl_quantize_weights_blockwise_multi(ctypes.addressof(arr), len(ws),
+                                                         _stream(stream)))
+    return qs, ss
+
+
+def quantize_act_groupwise(a: torch.Tensor, q: Optional[torch.Tensor] = None,
+                           scales: Optional[torch.Tensor] = None, stream=None):
+    """Per-token 1x128 E4M3 quantization of bf16 [m, k] -> (codes [m, k], scales [ceil(k/128), m])."""
+    _rowmajor(_dev(a, torch.bfloat16, "a"), "a")
+    m, k = a.shape
+    if q is None:
+        q = torch.empty(m, k, dtype=torch.uint8, device=a.device)
+    if scales is None:
+        scales = torch.empty((k + 127) // 128, m, dtype=torch.float32, device=a.device)
+    _dev(q, torch.uint8, "q")
+    _dev(scales, torch.float32, "scales")
+    if not q.is_contiguous():
+        raise ValueError("q must be dense [m, k]")
+    _check(load().fp8rl_quantize_act_groupwise(a.data_ptr(), m, k, a.stride(0), q.data_ptr(),
+                                               scales.data_ptr(), _stream(stream)))
+    return q, scales
+
+
+def quantize_kv_fp8(x: torch.Tensor, mode: int = FP8RL_KV_CALIBRATE,
+                    scales: Optional[torch.Tensor] = None, q: Optional[torch.Tensor] = None,
+                    stream=None):
+    """E4M3 K or V cache of bf16 [..., heads, head_dim] with per-head scales -> (codes, scales)."""
+    _dev(x, torch.bfloat16, "x")
+    if not x.is_contiguous() or x.dim() < 2:
+        raise ValueError("x must be a dense [..., heads, head_dim] tensor")
+    heads, hd = x.shape[-2], x.shape[-1]
+    rows = x.numel() // (heads * hd)
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        if mode == FP8RL_KV_GIVEN:
+            raise ValueError("FP8RL_KV_GIVEN needs scales")
+        scales = torch.empty(heads, dtype=torch.float32, device=x.device)
+    _dev(q, torch.uint8, "q")
+    _dev(scales, torch.float32, "scales")
+    _check(load().fp8rl_quantize_kv_fp8(x.data_ptr(), rows, heads, hd, mode, scales.data_ptr(),
+                                        q.data_ptr(), _stream(stream)))
+    return q, scales
+
+
+# ------------------------------------------------------------------ GEMMs --
+
+def gemm_w8a8_blockwise(qa, sa, qw, sw, y: Optional[torch.Tensor] = None, stream=None):
+    """Y = A W^T (bf16 [m, n]) from E4M3 codes and their block scales."""
+    _dev(qa, torch.uint8, "qa"); _dev(qw, torch.uint8, "qw")
+    _dev(sa, torch.float32, "sa"); _dev(sw, torch.float32, "sw")
+    m, k = qa.shape
+    n = qw.shape[0]
+    if y is None:
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=qa.device)
+    _rowmajor(_dev(y, torch.bfloat16, "y"), "y")
+    _check(load().fp8rl_gemm_w8a8_blockwise(qa.data_ptr(), sa.data_ptr(), qw.data_ptr(),
+                                            sw.data_ptr(), m, n, k, y.data_ptr(), y.stride(0),
+                                            _stream(stream)))
+    return y
+
+
+def grouped_gemm_w8a8_blockwise(qa, sa, qw, sw, offsets, y: Optional[torch.Tensor] = None,
+                                stream=None):
+    """Per-expert Y rows: rows [offsets[e], offsets[e+1]) use expert e's weights."""
+    _dev(qa, torch.uint8, "qa"); _dev(qw, torch.uint8, "qw")
+    _dev(sa, torch.float32, "sa"); _dev(sw, torch.float32, "sw")
+    _dev(offsets, torch.int32, "offsets")
+    m, k = qa.shape
+    e, n, _ = qw.shape
+    if y is None:
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=qa.device)
+    _dev(y, torch.bfloat16, "y")
+    _check(load().fp8rl_grouped_gemm_w8a8_blockwise(qa.data_ptr(), sa.data_ptr(), qw.data_ptr(),
+                                                    sw.data_ptr(), offsets.data_ptr(), e, m, n,
+                                                    k, y.data_ptr(), _stream(stream)))
+    return y
+
+
+# --------------------------------------------------------------------- TIS --
+
+def tis_weights(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_lo: float = 0.0,
+                w: Optional[torch.Tensor] = None, stream=None):
+    """Truncated importance weights min(exp(lt - lr), c_hi) (and >= c_lo when c_lo > 0)."""
+    _dev(logp_train, torch.float32, "logp_train")
+    _dev(logp_rollout, torch.float32, "logp_rollout")
+    n = logp_train.numel()
+    if logp_rollout.numel() != n:
+        raise ValueError("logp_train and logp_rollout must have the same size")
+    if w is None:
+        w = torch.empty_like(logp_train)
+    _dev(w, torch.float32, "w")
+    mp = 0
+    if mask is not None:
+        _dev(mask, torch.uint8, "mask")
+        mp = mask.data_ptr()
+    _check(load().fp8rl_tis_weights(logp_train.data_ptr(), logp_rollout.data_ptr(), mp, n,
+                                    float(c_hi), float(c_lo), w.data_ptr(), _stream(stream)))
+    return w
+
+
+def device_status(device: int = 0, clear: bool = True) -> int:
+    """Raises Fp8rlError(FP8RL_ERR_TIMEOUT) if a kernel hit a device-side wait limit."""
+    st = load().fp8rl_device_status(device, 1 if clear else 0)
+    _check(st)
+    return st

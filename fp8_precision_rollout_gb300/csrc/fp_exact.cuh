@@ -1,0 +1,277 @@
+// fp_exact.cuh -- exactly rounded binary32 building blocks of the hot path.
+//
+// Everything here is written against IEEE-754 round-to-nearest-even and uses
+// explicitly rounded operations (never contracted into FMAs by the compiler),
+// so that each function returns the same bits on the device and in a host
+// build compiled with -ffp-contract=off.
+//
+//  * quotient by a block scale, fl32(x / s), at the cost of one multiply and
+//    two FMAs: the correction step of P. Markstein ("Computation of elementary
+//    functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+//    1990; also "IA-64 and Elementary Functions", 2000).  With y = RN(1/s) and
+//    q0 = RN(x*y) within one ulp of x/s, r = x - q0*s is exact and
+//    RN(q0 + r*y) = RN(x/s), provided no intermediate underflows or
+//    overflows.  The fast form is used for scales in [2^-60, 2^126]: there,
+//    any |x| small enough for r to underflow (|x| < 2^-71) has |x/s| < 2^-11,
+//    whose E4M3 code is +-0 whatever the last bits of the quotient, so every
+//    code equals that of the IEEE quotient.  Other scales (tiny, huge,
+//    negative, non-finite) take IEEE division.
+//  * e^d correctly rounded to binary32 (the TIS weight): a float-float
+//    evaluation after Tang's table-driven method (P.T.P. Tang, "Table-driven
+//    implementation of the exponential function in IEEE floating-point
+//    arithmetic", ACM TOMS 15(2), 1989) with 32 table entries and a degree-6
+//    Taylor polynomial, accurate to ~2^-44 relative; inputs whose result lies
+//    within 2^-40 of a binary32 rounding boundary, or outside |d| <= 87, are
+//    recomputed with a double-double Taylor series (~2^-99) whose rounding is
+//    then exact.
+#pragma once
+
+#include <stdint.h>
+#include <math.h>
+
+#if defined(__CUDACC__)
+#define FP8RL_HD __host__ __device__ __forceinline__
+#else
+#define FP8RL_HD inline
+#endif
+
+namespace fp8rl {
+namespace fx {
+
+// ---- explicitly rounded primitives (device intrinsics; host IEEE ops) ------
+#if defined(__CUDA_ARCH__)
+FP8RL_HD float fadd(float a, float b) { return __fadd_rn(a, b); }
+FP8RL_HD float fsub(float a, float b) { return __fsub_rn(a, b); }
+FP8RL_HD float fmul(float a, float b) { return __fmul_rn(a, b); }
+FP8RL_HD float ffma(float a, float b, float c) { return __fmaf_rn(a, b, c); }
+FP8RL_HD float fdiv(float a, float b) { return __fdiv_rn(a, b); }
+FP8RL_HD float frcp(float a) { return __frcp_rn(a); }
+FP8RL_HD double dadd(double a, double b) { return __dadd_rn(a, b); }
+FP8RL_HD double dsub(double a, double b) { return __dsub_rn(a, b); }
+FP8RL_HD double dmul(double a, double b) { return __dmul_rn(a, b); }
+FP8RL_HD double dfma(double a, double b, double c) { return __fma_rn(a, b, c); }
+FP8RL_HD double ddiv(double a, double b) { return __ddiv_rn(a, b); }
+FP8RL_HD float d2f(double a) { return __double2float_rn(a); }
+FP8RL_HD uint32_t f2u(float f) { return __float_as_uint(f); }
+FP8RL_HD float u2f(uint32_t u) { return __uint_as_float(u); }
+#else
+FP8RL_HD float fadd(float a, float b) { return a + b; }
+FP8RL_HD float fsub(float a, float b) { return a - b; }
+FP8RL_HD float fmul(float a, float b) { return a * b; }
+FP8RL_HD float ffma(float a, float b, float c) { return fmaf(a, b, c); }
+FP8RL_HD float fdiv(float a, float b) { return a / b; }
+FP8RL_HD float frcp(float a) { return 1.0f / a; }
+FP8RL_HD double dadd(double a, double b) { return a + b; }
+FP8RL_HD double dsub(double a, double b) { return a - b; }
+FP8RL_HD double dmul(double a, double b) { return a * b; }
+FP8RL_HD double dfma(double a, double b, double c) { return fma(a, b, c); }
+FP8RL_HD double ddiv(double a, double b) { return a / b; }
+FP8RL_HD float d2f(double a) { return (float)a; }
+FP8RL_HD uint32_t f2u(float f) { union { float f; uint32_t u; } v; v.f = f; return v.u; }
+FP8RL_HD float u2f(uint32_t u) { union { float f; uint32_t u; } v; v.u = u; return v.f; }
+#endif
+
+// ---------------------------------------------------- quotient by a scale --
+
+// Per-scale set-up for the element map x -> fl32(x / s).
+struct ScaleDiv {
+  float s;
+  float y;     // RN(1/s) when mode == 1
+  int mode;    // 0: s == 0 (the value passes through); 1: Markstein; 2: IEEE divide
+};
+
+FP8RL_HD ScaleDiv make_scale_div(float s) {
+  ScaleDiv d;
+  d.s = s;
+  d.y = 0.0f;
+  if (s == 0.0f) {
+    d.mode = 0;
+  } else if (s >= 0x1p-60f && s <= 0x1p126f) {    // see the range note above
+    d.mode = 1;
+    d.y = frcp(s);
+  } else {
+    d.mode = 2;
+  }
+  return d;
+}
+
+// fl32(x / s) when mode == 1, |x / s| < 2^127 and |x| >= 2^-71; for smaller
+// |x| the result is within a few ulps of a quotient below 2^-11 (guarded
+// variant below for arbitrary caller scales).  The final copysign restores the sign
+// of a zero x, which the correction step would otherwise turn into +0.
+FP8RL_HD float markstein_quotient(float x, float s, float y) {
+  float q0 = fmul(x, y);
+  float r = ffma(-q0, s, x);
+  float q1 = ffma(r, y, q0);
+  return copysignf(q1, x);
+}
+
+// The element map's binary32 quotient under a prepared scale.  kGuard adds
+// the overflow guard needed when s is a caller-provided number rather than
+// amax/448 (then |x/s| may exceed 448 by any amount; every |q| >= 1024
+// saturates to 448 in E4M3 regardless of its exact value).
+template <bool kGuard>
+FP8RL_HD float scaled_quotient(float x, const ScaleDiv& d) {
+  if (d.mode == 1) {
+    float q = markstein_quotient(x, d.s, d.y);
+    if (kGuard) {
+      float q0 = fmul(x, d.y);
+      if (!(fabsf(q0) < 1024.0f)) q = q0;
+    }
+    return q;
+  }
+  if (d.mode == 0) return x;
+  return fdiv(x, d.s);
+}
+
+// ---------------------------------------------- correctly rounded e^d ------
+
+// 2^(j/32), j = 0..31, as float-float pairs (hi + lo), built on the host.
+struct Exp2Table {
+  float hi[32];
+  float lo[32];
+};
+
+FP8RL_HD void two_sum(float a, float b, float& s, float& e) {
+  s = fadd(a, b);
+  float bb = fsub(s, a);
+  e = fadd(fsub(a, fsub(s, bb)), fsub(b, bb));
+}
+FP8RL_HD void fast_two_sum(float a, float b, float& s, float& e) {  // needs |a| >= |b| or a == 0
+  s = fadd(a, b);
+  e = fsub(b, fsub(s, a));
+}
+FP8RL_HD void two_prod(float a, float b, float& p, float& e) {
+  p = fmul(a, b);
+  e = ffma(a, b, -p);
+}
+
+// Fast path.  Returns false when the input must take exp_rn32_slow (|d| > 87,
+// NaN, or a result too close to a rounding boundary to decide here).
+FP8RL_HD bool exp_rn32_fast(float d, const Exp2Table& T, float* out) {
+  if (!(fabsf(d) <= 87.0f)) return false;
+  // ln2/32 split in three: L1 has 12 significant bits so that k*L1 is exact
+  // for |k| < 2^12; L2 and L3 carry the next 48 bits.
+  const float kInvL = 0x1.715476p+5f;      // ~32/ln2; only sets the reduction range
+  const float L1 = 0x1.62ep-6f;
+  const float L2 = 0x1.0bfbe8p-20f;
+  const float L3 = 0x1.cf79acp-45f;
+  float kf = rintf(fmul(d, kInvL));
+  int k = (int)kf;
+  // r = d - k*ln2/32 as r_hi + r_lo, |r| <= ~ln2/64
+  float a = ffma(-kf, L1, d);                    // exact
+  float p_hi, p_lo;
+  two_prod(kf, L2, p_hi, p_lo);
+  float r_hi, e1;
+  two_sum(a, -p_hi, r_hi, e1);
+  float r_lo = fsub(fsub(e1, p_lo), fmul(kf, L3));
+  fast_two_sum(r_hi, r_lo, r_hi, r_lo);
+  // e^r - 1 = r + r^2/2 + r^3/6 + r^4/24 + r^5/120 + r^6/720 (+ < 2^-55)
+  float sq_hi, sq_lo;
+  two_prod(r_hi, r_hi, sq_hi, sq_lo);
+  float half = fmul(0.5f, sq_hi);                // exact
+  float half_lo = fadd(ffma(r_hi, r_lo, fmul(0.5f, sq_lo)), fmul(half, r_lo));
+  float t = ffma(r_hi, 1.0f / 720.0f, 1.0f / 120.0f);
+  t = ffma(r_hi, t, 1.0f / 24.0f);
+  t = ffma(r_hi, t, 1.0f / 6.0f);
+  float tail = fmul(fmul(sq_hi, r_hi), t);
+  float s1, e2;
+  fast_two_sum(r_hi, half, s1, e2);
+  float p_lo2 = fadd(fadd(fadd(e2, r_lo), half_lo), tail);
+  // 2^(j/32) * (1 + P), k = 32 m + j
+  int j = k & 31;
+  int m = (k - j) / 32;
+  float th = T.hi[j], tl = T.lo[j];
+  float m_hi, m_lo;
+  two_prod(th, s1, m_hi, m_lo);
+  float rest = fadd(fadd(fadd(m_lo, fmul(th, p_lo2)), tl), fmul(tl, fadd(s1, p_lo2)));
+  float y1, e3;
+  fast_two_sum(th, m_hi, y1, e3);
+  float yl0 = fadd(e3, rest);
+  float yh, yl;
+  fast_two_sum(y1, yl0, yh, yl);
+  // distance to the rounding boundary on yl's side of yh (yh > 0)
+  uint32_t b = f2u(yh);
+  float nb = u2f(yl >= 0.0f ? b + 1u : b - 1u);
+  float half_ulp = fmul(fsub(nb, yh), 0.5f);
+  float dist = fsub(fabsf(half_ulp), fabsf(yl));
+  if (dist <= fmul(yh, 0x1p-40f)) return false;
+  *out = fmul(yh, u2f((uint32_t)(m + 127) << 23));   // exact: the result is normal
+  return true;
+}
+
+// double-double helpers for the slow path
+struct dd { double hi, lo; };
+FP8RL_HD dd dd_fast(double a, double b) {
+  double s = dadd(a, b);
+  return dd{s, dsub(b, dsub(s, a))};
+}
+FP8RL_HD dd dd_two_sum(double a, double b) {
+  double s = dadd(a, b);
+  double bb = dsub(s, a);
+  return dd{s, dadd(dsub(a, dsub(s, bb)), dsub(b, bb))};
+}
+FP8RL_HD dd dd_mul(dd a, dd b) {
+  double p = dmul(a.hi, b.hi);
+  double e = dfma(a.hi, b.hi, -p);
+  e = dadd(e, dadd(dmul(a.hi, b.lo), dmul(a.lo, b.hi)));
+  return dd_fast(p, e);
+}
+FP8RL_HD dd dd_div_small(dd a, double i) {   // i a small positive integer
+  double q1 = ddiv(a.hi, i);
+  double rem = dfma(-q1, i, a.hi);             // exact
+  double q2 = ddiv(dadd(rem, a.lo), i);
+  return dd_fast(q1, q2);
+}
+FP8RL_HD dd dd_add_one(dd a) {
+  dd s = dd_two_sum(1.0, a.hi);
+  return dd_fast(s.hi, dadd(s.lo, a.lo));
+}
+
+// Correct binary32 rounding of the double-double value H + L.
+FP8RL_HD float dd_round_to_float(double H, double L) {
+  float f = d2f(H);
+  double fd = (double)f;
+  if (fd == H) return f;
+  float g = nextafterf(f, H > fd ? INFINITY : -INFINITY);
+  double mid;
+  if (isinf(f) || isinf(g))
+    mid = copysign(0x1p128 - 0x1p103, H);          // FLT_MAX / overflow boundary
+  else
+    mid = dmul(dadd(fd, (double)g), 0.5);          // exact
+  if (H == mid && L != 0.0) return ((L > 0.0) == (g > f)) ? g : f;
+  return f;
+}
+
+// Slow path: any binary32 d.
+FP8RL_HD float exp_rn32_slow(float d) {
+  if (d != d) return d;
+  if (d > 89.0f) return INFINITY;      // e^89 > 2^128: rounds to +inf
+  if (d < -104.0f) return 0.0f;        // e^-104 < 2^-150: rounds to +0
+  const double kLn2Hi = 0x1.62e42fefa39efp-1;     // ln 2 as a double-double
+  const double kLn2Lo = 0x1.abc9e3b39803fp-56;
+  double x = (double)d;
+  double k = rint(dmul(x, 0x1.71547652b82fep0));  // ~1/ln2; sets the reduction range
+  double p1 = dmul(k, kLn2Hi);
+  double p1e = dfma(k, kLn2Hi, -p1);
+  dd r = dd_two_sum(x, -p1);
+  r = dd_fast(r.hi, dsub(dsub(r.lo, p1e), dmul(k, kLn2Lo)));
+  // e^r, |r| <= ~0.35: Horner 1 + r/i (1 + r/(i+1)(...)) down from i = 27
+  dd p{1.0, 0.0};
+  for (int i = 27; i >= 1; --i) {
+    p = dd_mul(p, r);
+    p = dd_div_small(p, (double)i);
+    p = dd_add_one(p);
+  }
+  int ki = (int)k;
+  return dd_round_to_float(ldexp(p.hi, ki), ldexp(p.lo, ki));
+}
+
+FP8RL_HD float exp_rn32(float d, const Exp2Table& T) {
+  float e;
+  if (exp_rn32_fast(d, T, &e)) return e;
+  return exp_rn32_slow(d);
+}
+
+}  // namespace fx
+}  // namespace fp8rl

@@ -1,0 +1,634 @@
+// gemm.cu -- blockwise-scaled FP8 W8A8 GEMM on sm_103a tensor cores.
+//
+// FP8-RL summary, section 3.4.2 Phase 3: the rollout's linear layers multiply
+// dynamically quantized FP8 activations by the per-step re-quantized FP8
+// weights on FP8 tensor cores, accumulate in FP32 and emit BF16; section
+// 3.4.1 fixes the scale granularity (weights 128x128 blocks, activations
+// 1x128 groups) and names the MoE expert layers (fc1/fc2) as the grouped case.
+//
+//   Y[i, j] = bf16( sum_kb  sa[kb, i] * sw[j/128, kb] * P_kb[i, j] ),
+//   P_kb[i, j] = sum_{k in block kb} dec(qa[i, k]) * dec(qw[j, k]).
+//
+// The scales are arbitrary binary32 numbers (amax/448), so they cannot ride on
+// the hardware's block-scaled MMA (power-of-two UE8M0 scales per 32 K).  Each
+// 128-wide k-block is therefore one MMA group writing a fresh FP32 partial
+// P_kb into tensor memory; epilogue warps read it back (tcgen05.ld, 16 columns at a time), multiply
+// by sa*sw and add it into FP32 register accumulators.
+//
+// Kernel shape (one CTA per SM, persistent over output tiles):
+//   tile 128 (M) x 256 (N), k-block 128; 4-stage TMA ring of 48 KB stages
+//   (A 128x128 + B 256x128 bytes, 128-byte swizzle);
+//   warp 0     TMA producer (one elected lane),
+//   warp 1     TMEM allocator and MMA issuer (tcgen05.mma kind::f8f6f4,
+//              M=128 N=256 K=32, four per k-block, one elected lane),
+//   warps 2-9  epilogue: warp w reads TMEM lanes 32*(w%4).. and column half
+//              (w-2)/4, 128 FP32 accumulators per thread.
+//   TMEM: two 256-column partial buffers (all 512 columns), so the MMA of
+//   k-block kb+1 overlaps the promotion of kb.
+// Every wait on an mbarrier is bounded (1 s); on expiry the kernel records it
+// in the library's device status word, drains what it issued and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+
+namespace fp8rl {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int kThreads = 320;
+constexpr int kAStage = BM * BK;                 // 16 KB
+constexpr int kBStage = BN * BK;                 // 32 KB
+constexpr int kStageBytes = kAStage + kBStage;   // 48 KB
+constexpr int kMaxExperts = 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr int kMGroup = 16;                      // m-tiles per raster band (L2 reuse)
+
+// tcgen05 instruction descriptor, kind::f8f6f4: D = F32 (bits 4-5 = 1),
+// A = B = E4M3 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+struct SharedTail {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+  int32_t total_tiles;
+  int32_t pad;
+  int32_t seg[kMaxExperts + 1];      // grouped: clamped row offsets
+  int32_t tstart[kMaxExperts + 1];   // grouped: first tile of each expert
+  int32_t wsum[8];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * kStageBytes + sizeof(SharedTail);
+
+struct GemmArgs {
+  const float* sa;         // [KB, M] group-major activation scales
+  const float* sw;         // [E][NB][KB] weight block scales (E = 1 when dense)
+  __nv_bfloat16* y;
+  int64_t ldy;
+  int M, N, KB, NB;        // M = rows of A (m or m_total)
+  int num_m, num_n;        // num_m: dense only
+  const int32_t* offsets;  // grouped: [E+1] device
+  int E;                   // grouped: experts
+  uint32_t* status;        // library status word
+};
+
+// ------------------------------------------------------------ PTX wrappers --
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase of parity `parity`.  false: the CTA is aborting
+// (this wait timed out, or another role's did).
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile uint32_t* abort_flag,
+                                       uint32_t* status, uint32_t site) {
+  if (mbar_try(a, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(a, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (gtimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1u;
+        atomicOr(status, kStatusGemmTimeout);
+        atomicExch(status + 1, site);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t mbar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 64-bit shared-memory matrix descriptor, K-major operand with 128-byte
+// swizzle: start address >> 4 (bits 0-13), leading offset 1 (unused for this
+// layout), stride between 8-row groups 1024 B >> 4 (bits 32-45), descriptor
+// version 1 (bits 46-47), base offset 0, layout SWIZZLE_128B = 2 (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------- tile schedule --
+
+struct Tile {
+  int m0;        // first A row
+  int row_end;   // rows >= row_end are not part of this tile's problem
+  int n0;        // first output column
+  int brow;      // first B row (e * N + n0)
+  int e;         // expert (0 when dense)
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const SharedTail* st) {
+  Tile tl;
+  if (!kGrouped) {
+    const int per_band = kMGroup * g.num_n;
+    const int band = t / per_band;
+    const int first_m = band * kMGroup;
+    const int gs = min(kMGroup, g.num_m - first_m);
+    const int local = t - band * per_band;
+    const int mt = first_m + local % gs;
+    const int nt = local / gs;
+    tl.m0 = mt * BM;
+    tl.row_end = g.M;
+    tl.n0 = nt * BN;
+    tl.brow = tl.n0;
+    tl.e = 0;
+  } else {
+    int lo = 0, hi = g.E - 1;   // last expert whose first tile is <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (st->tstart[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int cnt = st->seg[e + 1] - st->seg[e];
+    const int mtiles = (cnt + BM - 1) / BM;
+    const int local = t - st->tstart[e];
+    const int mt = local % mtiles;
+    const int nt = local / mtiles;
+    tl.m0 = st->seg[e] + mt * BM;
+    tl.row_end = st->seg[e + 1];
+    tl.n0 = nt * BN;
+    tl.brow = e * g.N + tl.n0;
+    tl.e = e;
+  }
+  return tl;
+}
+
+// Grouped: copy the offsets (clamped to [0, M], made non-decreasing) and
+// build the exclusive prefix of tiles per expert, all threads cooperating.
+__device__ void build_expert_schedule(const GemmArgs& g, SharedTail* st) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i <= g.E; i += kThreads) st->seg[i] = min(max(g.offsets[i], 0), g.M);
+  __syncthreads();
+  if (tid == 0) {
+    for (int i = 1; i <= g.E; ++i) st->seg[i] = max(st->seg[i], st->seg[i - 1]);
+  }
+  __syncthreads();
+  int loc[4];
+  int sum = 0;
+  if (tid < 256) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = tid * 4 + j;
+      const int c = e < g.E ? st->seg[e + 1] - st->seg[e] : 0;
+      loc[j] = sum;
+      sum += ((c + BM - 1) / BM) * g.num_n;
+    }
+  }
+  // inclusive warp scan of the per-thread sums, then across the 8 warps
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (warp < 8 && lane == 31) st->wsum[warp] = incl;
+  __syncthreads();
+  if (tid < 256) {
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += st->wsum[w];
+    const int excl = before + incl - sum;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = tid * 4 + j;
+      if (e < g.E) st->tstart[e] = excl + loc[j];
+    }
+    if (tid == 255) {
+      int total = 0;
+      for (int w = 0; w < 8; ++w) total += st->wsum[w];
+      st->tstart[g.E] = total;
+      st->total_tiles = total;
+    }
+  }
+}
+
+// ----------------------------------------------------------------- kernel --
+
+template <bool kGrouped>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * kAStage;
+  SharedTail* st = reinterpret_cast<SharedTail*>(smem + STAGES * kStageBytes);
+  volatile uint32_t* abort_flag = &st->abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&st->full[s]), 1);
+      mbar_init(smem_u32(&st->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&st->tfull[b]), 1);
+      mbar_init(smem_u32(&st->tempty[b]), 8);
+    }
+    st->abort_flag = 0;
+    if (!kGrouped) st->total_tiles = g.num_m * g.num_n;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&st->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (kGrouped) build_expert_schedule(g, st);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = st->tmem_base;
+  const int total_tiles = st->total_tiles;
+  const int KB = g.KB;
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer --
+    uint32_t it = 0;
+    bool alive = true;
+    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+      const Tile tl = decode_tile<kGrouped>(t, g, st);
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1u;
+        bool okw = true;
+        if (lane == 0) okw = mbar_wait(smem_u32(&st->empty[s]), ph ^ 1u, abort_flag, g.status, 1);
+        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+        if (!okw) { alive = false; break; }
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&st->full[s]);
+          mbar_expect_tx(fb, kStageBytes);
+          tma_load_2d(smem_u32(sA + s * kAStage), &tmA, fb, kb * BK, tl.m0);
+          tma_load_2d(smem_u32(sB + s * kBStage), &tmB, fb, kb * BK, tl.brow);
+        }
+        __syncwarp();
+      }
+    }
+    if (!alive && lane == 0) {
+      // let the copies already issued land before the CTA can exit
+      const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+      for (uint32_t j = 1; j <= n; ++j) {
+        const uint32_t i2 = it - j;
+        volatile uint32_t never = 0;
+        mbar_wait(smem_u32(&st->full[i2 % STAGES]), (i2 / STAGES) & 1u, &never, g.status, 9);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    uint32_t it = 0, kit = 0;
+    bool alive = true;
+    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+      for (int kb = 0; kb < KB; ++kb, ++it, ++kit) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1u;
+        const int buf = kit & 1;
+        const uint32_t u = kit >> 1;
+        bool okw = true;
+        if (lane == 0) {
+          okw = mbar_wait(smem_u32(&st->tempty[buf]), (u & 1u) ^ 1u, abort_flag, g.status, 2) &&
+                mbar_wait(smem_u32(&st->full[s]), ph, abort_flag, g.status, 3);
+        }
+        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+        if (!okw) { alive = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+          const uint32_t a0 = smem_u32(sA + s * kAStage);
+          const uint32_t b0 = smem_u32(sB + s * kBStage);
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk)
+            mma_f8(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kk > 0 ? 1u : 0u);
+          mma_commit(smem_u32(&st->empty[s]));
+          mma_commit(smem_u32(&st->tfull[buf]));
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0 && it > 0) {
+      // the last stage release must have landed before the CTA exits
+      const uint32_t i2 = it - 1;
+      volatile uint32_t never = 0;
+      mbar_wait(smem_u32(&st->empty[i2 % STAGES]), (i2 / STAGES) & 1u, &never, g.status, 8);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;          // column half of the 256-wide tile
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t kit = 0;
+    bool alive = true;
+    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+      const Tile tl = decode_tile<kGrouped>(t, g, st);
+      const int row = tl.m0 + q * 32 + lane;
+      const bool row_ok = row < tl.row_end;
+      const int nbi = tl.n0 / 128 + h;
+      const float* swp = g.sw + ((int64_t)tl.e * g.NB + nbi) * KB;
+      const bool nb_ok = nbi < g.NB;
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      for (int kb = 0; kb < KB; ++kb, ++kit) {
+        const int buf = kit & 1;
+        const uint32_t u = kit >> 1;
+        const float sav = row_ok ? __ldg(g.sa + (int64_t)kb * g.M + row) : 0.0f;
+        const float swv = nb_ok ? __ldg(swp + kb) : 0.0f;
+        const float f = __fmul_rn(sav, swv);
+        bool okw = mbar_wait(smem_u32(&st->tfull[buf]), u & 1u, abort_flag, g.status, 4);
+        okw = __all_sync(0xFFFFFFFFu, okw);
+        if (!okw) { alive = false; break; }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + h * 128);
+        uint32_t p[16];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          tmem_ld16(taddr + c * 16, p);
+          tmem_wait_ld();
+          if (c == 7) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&st->tempty[buf]));
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            acc[c * 16 + j] = __fmaf_rn(__uint_as_float(p[j]), f, acc[c * 16 + j]);
+        }
+      }
+      if (!alive) break;
+      if (row_ok) {
+        __nv_bfloat16* yrow = g.y + (int64_t)row * g.ldy;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int col = tl.n0 + h * 128 + c * 8;
+          if (col < g.N) {
+            uint4 v;
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[c * 8 + 0], acc[c * 8 + 1]);
+            __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[c * 8 + 2], acc[c * 8 + 3]);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[c * 8 + 4], acc[c * 8 + 5]);
+            __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[c * 8 + 6], acc[c * 8 + 7]);
+            v.x = *reinterpret_cast<uint32_t*>(&b0);
+            v.y = *reinterpret_cast<uint32_t*>(&b1);
+            v.z = *reinterpret_cast<uint32_t*>(&b2);
+            v.w = *reinterpret_cast<uint32_t*>(&b3);
+            *reinterpret_cast<uint4*>(yrow + col) = v;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------- host --
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D uint8 map over a row-major [rows, inner] matrix, box [box_rows, 128],
+// 128-byte swizzle (the layout the UMMA descriptors above describe).
+fp8rl_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                      uint32_t box_rows, const char* what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FP8RL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(FP8RL_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what, (int)r);
+  return FP8RL_OK;
+}
+
+template <bool kGrouped>
+fp8rl_status set_smem_attr(const DeviceState* ds) {
+  static bool done[64] = {false};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ds->device < 64 && done[ds->device]) return FP8RL_OK;
+  if ((size_t)ds->max_smem_optin < kSmemBytes)
+    return fail(FP8RL_ERR_UNSUPPORTED_DEVICE, "GEMM needs %zu bytes of shared memory per block",
+                kSmemBytes);
+  fp8rl_status st = cuda_check(
+      cudaFuncSetAttribute(gemm_w8a8_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes),
+      "cudaFuncSetAttribute(gemm)");
+  if (st == FP8RL_OK && ds->device < 64) done[ds->device] = true;
+  return st;
+}
+
+fp8rl_status check_common(const uint8_t* qa, const float* sa, const uint8_t* qw, const float* sw,
+                          int64_t n, int64_t k, const void* y) {
+  if (!qa || !sa || !qw || !sw || !y) return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (k < 128 || k % 128)
+    return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "k must be a positive multiple of 128 (k=%lld)",
+                (long long)k);
+  if (n < 16 || n % 16)
+    return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "n must be a positive multiple of 16 (n=%lld)",
+                (long long)n);
+  if (k > INT32_MAX / 2 || n > INT32_MAX / 2)
+    return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "n or k too large");
+  if (!aligned(qa, 16) || !aligned(qw, 16) || !aligned(y, 16) || !aligned(sa, 4) ||
+      !aligned(sw, 4))
+    return fail(FP8RL_ERR_ALIGNMENT, "qa, qw and y must be 16-byte aligned");
+  return FP8RL_OK;
+}
+
+}  // namespace
+}  // namespace fp8rl
+
+using namespace fp8rl;
+
+extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float* sa,
+                                                  const uint8_t* qw, const float* sw, int64_t m,
+                                                  int64_t n, int64_t k, void* y, int64_t ldy,
+                                                  cudaStream_t stream) {
+  fp8rl_status st = check_common(qa, sa, qw, sw, n, k, y);
+  if (st != FP8RL_OK) return st;
+  if (m < 0 || m > INT32_MAX - BM) return fail(FP8RL_ERR_INVALID_ARG, "m out of range");
+  if (ldy < n || ldy % 8) return fail(FP8RL_ERR_ALIGNMENT, "need ldy >= n and ldy % 8 == 0");
+  if (m == 0) return ok();
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FP8RL_OK) return st;
+  if ((st = set_smem_attr<false>(ds)) != FP8RL_OK) return st;
+  CUtensorMap tmA, tmB;
+  if ((st = make_map(&tmA, qa, (uint64_t)k, (uint64_t)m, BM, "A")) != FP8RL_OK) return st;
+  if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)n, BN, "W")) != FP8RL_OK) return st;
+  GemmArgs g;
+  g.sa = sa;
+  g.sw = sw;
+  g.y = reinterpret_cast<__nv_bfloat16*>(y);
+  g.ldy = ldy;
+  g.M = (int)m;
+  g.N = (int)n;
+  g.KB = (int)(k / BK);
+  g.NB = (int)((n + 127) / 128);
+  g.num_m = (int)((m + BM - 1) / BM);
+  g.num_n = (int)((n + BN - 1) / BN);
+  g.offsets = nullptr;
+  g.E = 1;
+  g.status = ds->status;
+  const int64_t tiles = (int64_t)g.num_m * g.num_n;
+  if (tiles > INT32_MAX) return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "too many tiles");
+  const int grid = (int)std::min<int64_t>(tiles, ds->sm_count);
+  gemm_w8a8_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+  st = cuda_check(cudaGetLastError(), "gemm_w8a8_kernel launch");
+  return st == FP8RL_OK ? ok() : st;
+}
+
+extern "C" fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, const float* sa,
+                                                          const uint8_t* qw, const float* sw,
+                                                          const int32_t* offsets,
+                                                          int32_t num_experts, int64_t m_total,
+                                                          int64_t n, int64_t k, void* y,
+                                                          cudaStream_t stream) {
+  fp8rl_status st = check_common(qa, sa, qw, sw, n, k, y);
+  if (st != FP8RL_OK) return st;
+  if (!offsets) return fail(FP8RL_ERR_INVALID_ARG, "null offsets");
+  if (!aligned(offsets, 4)) return fail(FP8RL_ERR_ALIGNMENT, "offsets must be 4-byte aligned");
+  if (num_experts < 1 || num_experts > kMaxExperts)
+    return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "need 1 <= num_experts <= %d", kMaxExperts);
+  if (n % 128) return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "grouped GEMM needs n % 128 == 0");
+  if (m_total < 0 || m_total > INT32_MAX - BM) return fail(FP8RL_ERR_INVALID_ARG, "m_total out of range");
+  if ((int64_t)num_experts * n > INT32_MAX) return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "e*n too large");
+  if (m_total == 0) return ok();
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FP8RL_OK) return st;
+  if ((st = set_smem_attr<true>(ds)) != FP8RL_OK) return st;
+  CUtensorMap tmA, tmB;
+  if ((st = make_map(&tmA, qa, (uint64_t)k, (uint64_t)m_total, BM, "A")) != FP8RL_OK) return st;
+  if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)num_experts * n, BN, "W")) != FP8RL_OK)
+    return st;
+  GemmArgs g;
+  g.sa = sa;
+  g.sw = sw;
+  g.y = reinterpret_cast<__nv_bfloat16*>(y);
+  g.ldy = n;
+  g.M = (int)m_total;
+  g.N = (int)n;
+  g.KB = (int)(k / BK);
+  g.NB = (int)(n / 128);
+  g.num_m = 0;
+  g.num_n = (int)((n + BN - 1) / BN);
+  g.offsets = offsets;
+  g.E = num_experts;
+  g.status = ds->status;
+  const int64_t bound = ((m_total + BM - 1) / BM + num_experts) * (int64_t)g.num_n;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(bound, ds->sm_count));
+  gemm_w8a8_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+  st = cuda_check(cudaGetLastError(), "grouped gemm_w8a8_kernel launch");
+  return st == FP8RL_OK ? ok() : st;
+}

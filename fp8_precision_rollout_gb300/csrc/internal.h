@@ -1,0 +1,40 @@
+// internal.h -- host-side plumbing shared by the fp8rl translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp8rl.h"
+
+namespace fp8rl {
+
+// Records a message for fp8rl_last_error() and returns `st`.
+fp8rl_status fail(fp8rl_status st, const char* fmt, ...);
+// Clears the thread's last error and returns FP8RL_OK.
+fp8rl_status ok();
+// Maps a CUDA error to FP8RL_ERR_CUDA with context; FP8RL_OK for cudaSuccess.
+fp8rl_status cuda_check(cudaError_t e, const char* what);
+
+// Per-device state, created on first use (current device).
+struct DeviceState {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  int max_smem_optin = 0;
+  // library workspace (device memory, zero-initialised at creation)
+  uint32_t* status = nullptr;      // [0]: timeout flags, [1]: where the wait gave up
+  uint32_t* kv_amax = nullptr;     // 256 calibration slots (float bits)
+};
+
+// Looks up (creating if needed) the state of the current device and checks
+// that it is an sm_103 part.  On failure returns a status (message set).
+fp8rl_status device_state(DeviceState** out);
+
+// Device status word bits.
+enum : uint32_t {
+  kStatusGemmTimeout = 1u << 0,
+};
+
+inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace fp8rl

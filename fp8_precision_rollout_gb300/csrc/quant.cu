@@ -1,0 +1,404 @@
+// quant.cu -- the bandwidth-bound quantizers of the FP8 rollout hot path.
+//
+//   * blockwise 128x128 weight re-quantization, single tensor and a whole
+//     model's tensors in one launch (FP8-RL summary, sections 3.4.1 and 3.4.2
+//     Phase 2 step 2),
+//   * per-token 1x128-group activation quantization (sections 3.4.1/3.4.2
+//     Phase 3, dynamic quantization),
+//   * FP8 E4M3 KV-cache quantization with per-head scales, given or
+//     calibrated from the tensor (section 3.4.4).
+//
+// All three apply one element map: scale = fl32(amax/448), code =
+// E4M3_RNE_satfinite(fl32(x/scale)).  The binary32 quotient is formed with
+// the exact Markstein correction of fp_exact.cuh and rounded to E4M3 by the
+// hardware conversion (cvt.rn.satfinite.e4m3x2.f32).  Every kernel reads its
+// input once with 16-byte non-allocating loads and writes packed 8-byte code
+// vectors; amax is a bf16x2 max over |x| bit patterns, then warp shuffles.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "fp_exact.cuh"
+#include "internal.h"
+
+namespace fp8rl {
+namespace {
+
+using fx::ScaleDiv;
+using fx::make_scale_div;
+using fx::scaled_quotient;
+
+// ------------------------------------------------------------ device bits --
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// max |x| over the 8 bf16 of a 16-byte vector, folded into a bf16x2 running max
+__device__ __forceinline__ uint32_t absmax8(uint32_t m, const uint4& v) {
+  m = bf16x2_max(m, v.x & 0x7FFF7FFFu);
+  m = bf16x2_max(m, v.y & 0x7FFF7FFFu);
+  m = bf16x2_max(m, v.z & 0x7FFF7FFFu);
+  m = bf16x2_max(m, v.w & 0x7FFF7FFFu);
+  return m;
+}
+
+__device__ __forceinline__ float bf16x2_maxf(uint32_t m) {
+  return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+
+// two binary32 -> two E4M3 codes (lo in the low byte), RNE, saturating
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+// the element map over one bf16x2 word -> 2 codes
+template <bool kGuard>
+__device__ __forceinline__ uint32_t quant2(uint32_t w, const ScaleDiv& sd) {
+  float x0 = __uint_as_float(w << 16);
+  float x1 = __uint_as_float(w & 0xFFFF0000u);
+  return cvt_e4m3x2(scaled_quotient<kGuard>(x0, sd), scaled_quotient<kGuard>(x1, sd));
+}
+
+// 8 bf16 -> 8 codes packed in a uint2
+template <bool kGuard>
+__device__ __forceinline__ uint2 quant8(const uint4& v, const ScaleDiv& sd) {
+  uint2 r;
+  r.x = quant2<kGuard>(v.x, sd) | (quant2<kGuard>(v.y, sd) << 16);
+  r.y = quant2<kGuard>(v.z, sd) | (quant2<kGuard>(v.w, sd) << 16);
+  return r;
+}
+
+__device__ __forceinline__ float warp_max(float v, int width) {
+  for (int o = width >> 1; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// -------------------------------------------------- 128x128 weight blocks --
+
+constexpr int kMaxDescs = 256;
+
+struct WQDesc {
+  const uint16_t* w;
+  uint8_t* q;
+  float* scales;
+  int64_t n, k, ldw, ldq;
+  int32_t kb;      // ceil(k/128)
+  int32_t pad;
+};
+
+struct WQParams {
+  int32_t count;
+  int32_t start[kMaxDescs + 1];   // first block id of each tensor; start[count] = total
+  WQDesc d[kMaxDescs];
+};
+
+// One CTA of 256 threads per 128x128 block.  Warp w, half-warp h handles rows
+// 2w + h + 16i (i = 0..7); lane c of the half-warp the 16-byte column chunk c.
+// The block stays in registers between the max and the quantization: one HBM
+// read and one write per element.
+__global__ void __launch_bounds__(256) wquant_kernel(const __grid_constant__ WQParams p) {
+  const int b = blockIdx.x;
+  int lo = 0, hi = p.count - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (p.start[mid] <= b) lo = mid; else hi = mid - 1;
+  }
+  const WQDesc& d = p.d[lo];
+  const int local = b - p.start[lo];
+  const int bi = local / d.kb, bj = local - (local / d.kb) * d.kb;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t r0 = (int64_t)bi * 128 + warp * 2 + (lane >> 4);
+  const int64_t col = (int64_t)bj * 128 + (lane & 15) * 8;
+  const bool full = ((int64_t)bi * 128 + 128 <= d.n) && ((int64_t)bj * 128 + 128 <= d.k);
+  const bool col_ok = col < d.k;
+
+  uint4 v[8];
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t r = r0 + 16 * i;
+    if (full || (col_ok && r < d.n)) {
+      v[i] = ld_stream(d.w + r * d.ldw + col);
+    } else {
+      v[i] = make_uint4(0, 0, 0, 0);
+    }
+    m2 = absmax8(m2, v[i]);
+  }
+  float amax = warp_max(bf16x2_maxf(m2), 32);
+  __shared__ float red[8];
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const float s = fx::fdiv(amax, 448.0f);
+  if (tid == 0) d.scales[(int64_t)bi * d.kb + bj] = s;
+  const ScaleDiv sd = make_scale_div(s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t r = r0 + 16 * i;
+    if (full || (col_ok && r < d.n)) {
+      *reinterpret_cast<uint2*>(d.q + r * d.ldq + col) = quant8<false>(v[i], sd);
+    }
+  }
+}
+
+fp8rl_status check_wdesc(const fp8rl_wdesc& d, int idx) {
+  if (!d.w || !d.q || !d.scales)
+    return fail(FP8RL_ERR_INVALID_ARG, "weight tensor %d: null pointer", idx);
+  if (d.n < 1 || d.k < 1 || d.ldw < d.k || d.ldq < d.k)
+    return fail(FP8RL_ERR_INVALID_ARG,
+                "weight tensor %d: need n, k >= 1, ldw >= k, ldq >= k (n=%lld k=%lld ldw=%lld ldq=%lld)",
+                idx, (long long)d.n, (long long)d.k, (long long)d.ldw, (long long)d.ldq);
+  if (d.k % 8 || d.ldw % 8 || d.ldq % 8)
+    return fail(FP8RL_ERR_ALIGNMENT, "weight tensor %d: k, ldw and ldq must be multiples of 8", idx);
+  if (!aligned(d.w, 16) || !aligned(d.q, 8) || !aligned(d.scales, 4))
+    return fail(FP8RL_ERR_ALIGNMENT, "weight tensor %d: w must be 16-byte, q 8-byte aligned", idx);
+  int64_t blocks = ((d.n + 127) / 128) * ((d.k + 127) / 128);
+  if (blocks > (int64_t)1 << 30)
+    return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "weight tensor %d: too many blocks", idx);
+  return FP8RL_OK;
+}
+
+// ------------------------------------------------ 1x128 activation groups --
+
+// A warp task is 8 consecutive groups of one row; 4 lanes per group, each lane
+// 4 x 16-byte chunks (chunk slot + 4i of its group).  Scales go to the
+// group-major array scales[g * m + r].
+__global__ void __launch_bounds__(256) aquant_kernel(const uint16_t* __restrict__ a, int64_t m,
+                                                     int64_t k, int64_t lda,
+                                                     uint8_t* __restrict__ q,
+                                                     float* __restrict__ scales,
+                                                     int64_t n_tasks, int octets, int kb) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int slot = lane & 3;
+  for (int64_t task = gw; task < n_tasks; task += nw) {
+    const int64_t r = task / octets;
+    const int o = (int)(task - r * octets);
+    const int g = o * 8 + (lane >> 2);
+    const int64_t gcol = (int64_t)g * 128;
+    const uint16_t* arow = a + r * lda;
+    uint4 v[4];
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t col = gcol + (slot + 4 * i) * 8;
+      v[i] = (g < kb && col < k) ? ld_stream(arow + col) : make_uint4(0, 0, 0, 0);
+      m2 = absmax8(m2, v[i]);
+    }
+    const float amax = warp_max(bf16x2_maxf(m2), 4);
+    const float s = fx::fdiv(amax, 448.0f);
+    if (slot == 0 && g < kb) scales[(int64_t)g * m + r] = s;
+    const ScaleDiv sd = make_scale_div(s);
+    uint8_t* qrow = q + r * k;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t col = gcol + (slot + 4 * i) * 8;
+      if (g < kb && col < k) *reinterpret_cast<uint2*>(qrow + col) = quant8<false>(v[i], sd);
+    }
+  }
+}
+
+// ----------------------------------------------------------- KV cache -----
+
+// Thread t of a 256-thread CTA owns 16-byte vector slot t % vpr of a row
+// (vpr = heads*head_dim/8 vectors per row), so its head is fixed; the CTA
+// walks rows 256/vpr at a time with a grid stride.
+struct KVMap {
+  int vpr, rpp, hd;
+  __device__ __forceinline__ bool active(int t) const { return t / vpr < rpp; }
+};
+
+__global__ void __launch_bounds__(256) kv_amax_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                      KVMap mp, uint32_t* __restrict__ amax_out,
+                                                      int heads) {
+  __shared__ uint32_t sm[256];
+  const int t = threadIdx.x;
+  sm[t] = 0;
+  __syncthreads();
+  if (mp.active(t)) {
+    const int v = t % mp.vpr, rsub = t / mp.vpr;
+    const int64_t row_elems = (int64_t)mp.vpr * 8;
+    const int64_t stride = (int64_t)gridDim.x * mp.rpp;
+    uint32_t m2 = 0;
+    int64_t r = (int64_t)blockIdx.x * mp.rpp + rsub;
+    for (; r + 3 * stride < rows; r += 4 * stride) {
+      uint4 a0 = ld_stream(x + r * row_elems + v * 8);
+      uint4 a1 = ld_stream(x + (r + stride) * row_elems + v * 8);
+      uint4 a2 = ld_stream(x + (r + 2 * stride) * row_elems + v * 8);
+      uint4 a3 = ld_stream(x + (r + 3 * stride) * row_elems + v * 8);
+      m2 = absmax8(absmax8(absmax8(absmax8(m2, a0), a1), a2), a3);
+    }
+    for (; r < rows; r += stride) m2 = absmax8(m2, ld_stream(x + r * row_elems + v * 8));
+    const float am = bf16x2_maxf(m2);
+    atomicMax(&sm[(v * 8) / mp.hd], __float_as_uint(am));   // non-negative: int order = float order
+  }
+  __syncthreads();
+  if (t < heads && sm[t] != 0) atomicMax(&amax_out[t], sm[t]);
+}
+
+template <bool kCalibrated>
+__global__ void __launch_bounds__(256) kv_quant_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                       KVMap mp, const float* __restrict__ scales_in,
+                                                       const uint32_t* __restrict__ amax_ws,
+                                                       float* __restrict__ scales_out,
+                                                       uint8_t* __restrict__ q, int heads) {
+  const int t = threadIdx.x;
+  if (kCalibrated && blockIdx.x == 0 && t < heads)
+    scales_out[t] = fx::fdiv(__uint_as_float(amax_ws[t]), 448.0f);
+  if (!mp.active(t)) return;
+  const int v = t % mp.vpr, rsub = t / mp.vpr;
+  const int h = (v * 8) / mp.hd;
+  const float s = kCalibrated ? fx::fdiv(__uint_as_float(amax_ws[h]), 448.0f) : scales_in[h];
+  const ScaleDiv sd = make_scale_div(s);
+  const int64_t row_elems = (int64_t)mp.vpr * 8;
+  const int64_t stride = (int64_t)gridDim.x * mp.rpp;
+  int64_t r = (int64_t)blockIdx.x * mp.rpp + rsub;
+  for (; r + 3 * stride < rows; r += 4 * stride) {
+    uint4 a0 = ld_stream(x + r * row_elems + v * 8);
+    uint4 a1 = ld_stream(x + (r + stride) * row_elems + v * 8);
+    uint4 a2 = ld_stream(x + (r + 2 * stride) * row_elems + v * 8);
+    uint4 a3 = ld_stream(x + (r + 3 * stride) * row_elems + v * 8);
+    *reinterpret_cast<uint2*>(q + r * row_elems + v * 8) = quant8<!kCalibrated>(a0, sd);
+    *reinterpret_cast<uint2*>(q + (r + stride) * row_elems + v * 8) = quant8<!kCalibrated>(a1, sd);
+    *reinterpret_cast<uint2*>(q + (r + 2 * stride) * row_elems + v * 8) = quant8<!kCalibrated>(a2, sd);
+    *reinterpret_cast<uint2*>(q + (r + 3 * stride) * row_elems + v * 8) = quant8<!kCalibrated>(a3, sd);
+  }
+  for (; r < rows; r += stride)
+    *reinterpret_cast<uint2*>(q + r * row_elems + v * 8) =
+        quant8<!kCalibrated>(ld_stream(x + r * row_elems + v * 8), sd);
+}
+
+int grid_for(int64_t work_ctas, const DeviceState* ds, int per_sm) {
+  int64_t cap = (int64_t)ds->sm_count * per_sm;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(work_ctas, cap));
+}
+
+}  // namespace
+}  // namespace fp8rl
+
+using namespace fp8rl;
+
+extern "C" fp8rl_status fp8rl_quantize_weights_blockwise_multi(const fp8rl_wdesc* descs,
+                                                               int32_t count,
+                                                               cudaStream_t stream) {
+  if (count < 0 || (count > 0 && !descs))
+    return fail(FP8RL_ERR_INVALID_ARG, "descs must be a host array of count >= 0 descriptors");
+  for (int i = 0; i < count; ++i) {
+    fp8rl_status st = check_wdesc(descs[i], i);
+    if (st != FP8RL_OK) return st;
+  }
+  if (count == 0) return ok();
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  if (st != FP8RL_OK) return st;
+  static WQParams p;   // large: keep off the stack; guarded by the launch sequence below
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int base = 0; base < count; base += kMaxDescs) {
+    const int c = std::min(kMaxDescs, count - base);
+    std::memset(&p, 0, sizeof(p));
+    p.count = c;
+    int64_t total = 0;
+    for (int i = 0; i < c; ++i) {
+      const fp8rl_wdesc& d = descs[base + i];
+      const int64_t kb = (d.k + 127) / 128;
+      p.start[i] = (int32_t)total;
+      p.d[i] = WQDesc{reinterpret_cast<const uint16_t*>(d.w), d.q, d.scales, d.n, d.k,
+                      d.ldw, d.ldq, (int32_t)kb, 0};
+      total += ((d.n + 127) / 128) * kb;
+      if (total > INT32_MAX)
+        return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "more than 2^31 blocks in one launch");
+    }
+    p.start[c] = (int32_t)total;
+    wquant_kernel<<<(unsigned)total, 256, 0, stream>>>(p);
+    st = cuda_check(cudaGetLastError(), "wquant_kernel launch");
+    if (st != FP8RL_OK) return st;
+  }
+  return ok();
+}
+
+extern "C" fp8rl_status fp8rl_quantize_weights_blockwise(const void* w, int64_t n, int64_t k,
+                                                         int64_t ldw, uint8_t* q, int64_t ldq,
+                                                         float* scales, cudaStream_t stream) {
+  fp8rl_wdesc d{w, q, scales, n, k, ldw, ldq};
+  return fp8rl_quantize_weights_blockwise_multi(&d, 1, stream);
+}
+
+extern "C" fp8rl_status fp8rl_quantize_act_groupwise(const void* a, int64_t m, int64_t k,
+                                                     int64_t lda, uint8_t* q, float* scales,
+                                                     cudaStream_t stream) {
+  if (!a || !q || !scales) return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (m < 1 || k < 1 || lda < k)
+    return fail(FP8RL_ERR_INVALID_ARG, "need m, k >= 1 and lda >= k (m=%lld k=%lld lda=%lld)",
+                (long long)m, (long long)k, (long long)lda);
+  if (k % 8 || lda % 8) return fail(FP8RL_ERR_ALIGNMENT, "k and lda must be multiples of 8");
+  if (!aligned(a, 16) || !aligned(q, 8) || !aligned(scales, 4))
+    return fail(FP8RL_ERR_ALIGNMENT, "a must be 16-byte and q 8-byte aligned");
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  if (st != FP8RL_OK) return st;
+  const int kb = (int)((k + 127) / 128);
+  const int octets = (kb + 7) / 8;
+  const int64_t tasks = m * octets;
+  const int64_t ctas = (tasks + 7) / 8;
+  aquant_kernel<<<grid_for(ctas, ds, 8), 256, 0, stream>>>(
+      reinterpret_cast<const uint16_t*>(a), m, k, lda, q, scales, tasks, octets, kb);
+  st = cuda_check(cudaGetLastError(), "aquant_kernel launch");
+  return st == FP8RL_OK ? ok() : st;
+}
+
+extern "C" fp8rl_status fp8rl_quantize_kv_fp8(const void* x, int64_t rows, int32_t heads,
+                                              int32_t head_dim, int32_t mode, float* scales,
+                                              uint8_t* q, cudaStream_t stream) {
+  if (!x || !scales || !q) return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (rows < 0 || heads < 1 || head_dim < 1)
+    return fail(FP8RL_ERR_INVALID_ARG, "need rows >= 0, heads >= 1, head_dim >= 1");
+  if (mode != FP8RL_KV_GIVEN && mode != FP8RL_KV_CALIBRATE)
+    return fail(FP8RL_ERR_INVALID_ARG, "mode must be FP8RL_KV_GIVEN or FP8RL_KV_CALIBRATE");
+  if (head_dim % 8) return fail(FP8RL_ERR_ALIGNMENT, "head_dim must be a multiple of 8");
+  if ((int64_t)heads * head_dim > 2048 || heads > 256)
+    return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "need heads*head_dim <= 2048 and heads <= 256");
+  if (!aligned(x, 16) || !aligned(q, 8) || !aligned(scales, 4))
+    return fail(FP8RL_ERR_ALIGNMENT, "x must be 16-byte and q 8-byte aligned");
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  if (st != FP8RL_OK) return st;
+  KVMap mp;
+  mp.vpr = heads * head_dim / 8;
+  mp.rpp = 256 / mp.vpr;
+  mp.hd = head_dim;
+  const int64_t ctas = rows > 0 ? (rows + mp.rpp - 1) / mp.rpp : 1;
+  const int grid = grid_for(ctas, ds, 8);
+  const uint16_t* xb = reinterpret_cast<const uint16_t*>(x);
+  if (mode == FP8RL_KV_CALIBRATE) {
+    st = cuda_check(cudaMemsetAsync(ds->kv_amax, 0, sizeof(uint32_t) * heads, stream),
+                    "clearing calibration slots");
+    if (st != FP8RL_OK) return st;
+    kv_amax_kernel<<<grid, 256, 0, stream>>>(xb, rows, mp, ds->kv_amax, heads);
+    st = cuda_check(cudaGetLastError(), "kv_amax_kernel launch");
+    if (st != FP8RL_OK) return st;
+    kv_quant_kernel<true><<<grid, 256, 0, stream>>>(xb, rows, mp, nullptr, ds->kv_amax, scales,
+                                                    q, heads);
+  } else {
+    kv_quant_kernel<false><<<grid, 256, 0, stream>>>(xb, rows, mp, scales, nullptr, nullptr, q,
+                                                     heads);
+  }
+  st = cuda_check(cudaGetLastError(), "kv_quant_kernel launch");
+  return st == FP8RL_OK ? ok() : st;
+}

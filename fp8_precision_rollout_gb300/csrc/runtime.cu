@@ -1,0 +1,101 @@
+// runtime.cu -- error reporting, per-device state and workspace, status word.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+
+namespace fp8rl {
+
+namespace {
+thread_local std::string g_last_error;
+std::mutex g_mu;
+constexpr int kMaxDevices = 64;
+DeviceState g_states[kMaxDevices];
+constexpr size_t kWorkspaceBytes = 4096;
+}  // namespace
+
+fp8rl_status fail(fp8rl_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+fp8rl_status ok() {
+  g_last_error.clear();
+  return FP8RL_OK;
+}
+
+fp8rl_status cuda_check(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return FP8RL_OK;
+  return fail(FP8RL_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+fp8rl_status device_state(DeviceState** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_check(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FP8RL_ERR_UNSUPPORTED_DEVICE, "device %d", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_states[dev];
+  if (st.device < 0) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_check(e, "cudaGetDeviceProperties");
+    if (!(prop.major == 10 && prop.minor == 3))
+      return fail(FP8RL_ERR_UNSUPPORTED_DEVICE,
+                  "fp8rl is built for sm_103a (GB300); device %d is sm_%d%d (%s)", dev,
+                  prop.major, prop.minor, prop.name);
+    void* ws = nullptr;
+    e = cudaMalloc(&ws, kWorkspaceBytes);
+    if (e != cudaSuccess) return cuda_check(e, "cudaMalloc(workspace)");
+    e = cudaMemset(ws, 0, kWorkspaceBytes);
+    if (e != cudaSuccess) return cuda_check(e, "cudaMemset(workspace)");
+    st.sm_count = prop.multiProcessorCount;
+    st.cc_major = prop.major;
+    st.cc_minor = prop.minor;
+    st.max_smem_optin = (int)prop.sharedMemPerBlockOptin;
+    st.status = reinterpret_cast<uint32_t*>(ws);
+    st.kv_amax = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + 1024);
+    st.device = dev;
+  }
+  *out = &st;
+  return FP8RL_OK;
+}
+
+}  // namespace fp8rl
+
+using namespace fp8rl;
+
+extern "C" int32_t fp8rl_version(void) { return FP8RL_VERSION; }
+
+extern "C" const char* fp8rl_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" fp8rl_status fp8rl_device_status(int32_t device, int32_t clear) {
+  int prev = -1;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return cuda_check(e, "cudaGetDevice");
+  if (device != prev) {
+    e = cudaSetDevice(device);
+    if (e != cudaSuccess) return cuda_check(e, "cudaSetDevice");
+  }
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  uint32_t words[2] = {0, 0};
+  if (st == FP8RL_OK) {
+    e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(words, ds->status, sizeof(words), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && clear) e = cudaMemset(ds->status, 0, sizeof(words));
+    st = cuda_check(e, "reading the device status word");
+  }
+  if (device != prev) cudaSetDevice(prev);
+  if (st != FP8RL_OK) return st;
+  if (words[0] & kStatusGemmTimeout)
+    return fail(FP8RL_ERR_TIMEOUT, "a GEMM pipeline wait hit its time limit (site %u)", words[1]);
+  return ok();
+}

@@ -1,0 +1,100 @@
+// tis.cu -- token-level truncated importance-sampling weights.
+//
+// FP8-RL summary, section 3.4.3: the weight of a token is the ratio of the
+// training policy's probability to the FP8 rollout policy's,
+// w = exp(logp_train - logp_rollout), truncated at C (= 2 in all of the pages'
+// experiments; the same section also states the two-sided range [1/C, C]).
+// Here d = fl32(logp_train - logp_rollout), e = RN32(e^d) exactly (see
+// fp_exact.cuh), w = min(e, c_hi), then max(w, c_lo) when c_lo > 0, NaN kept,
+// and w = 0 for masked-out tokens.  Elementwise and HBM-bound: 16-byte loads
+// of 4 tokens per thread, grid-stride.
+#include <cmath>
+
+#include "fp_exact.cuh"
+#include "internal.h"
+
+namespace fp8rl {
+namespace {
+
+__device__ __forceinline__ float tis_one(float lt, float lr, float c_hi, float c_lo,
+                                         const fx::Exp2Table& T) {
+  const float d = fx::fsub(lt, lr);
+  const float e = fx::exp_rn32(d, T);
+  float w = (e > c_hi) ? c_hi : e;
+  if (c_lo > 0.0f && e < c_lo) w = c_lo;
+  return w;
+}
+
+__global__ void __launch_bounds__(256) tis_kernel(const float* __restrict__ lt,
+                                                  const float* __restrict__ lr,
+                                                  const uint8_t* __restrict__ mask, int64_t n,
+                                                  float c_hi, float c_lo, float* __restrict__ w,
+                                                  const __grid_constant__ fx::Exp2Table T) {
+  const int64_t n4 = n >> 2;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(lt) + i);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(lr) + i);
+    float4 r;
+    r.x = tis_one(a.x, b.x, c_hi, c_lo, T);
+    r.y = tis_one(a.y, b.y, c_hi, c_lo, T);
+    r.z = tis_one(a.z, b.z, c_hi, c_lo, T);
+    r.w = tis_one(a.w, b.w, c_hi, c_lo, T);
+    if (mask) {
+      const uint32_t mk = __ldg(reinterpret_cast<const unsigned int*>(mask) + i);
+      if (!(mk & 0xFFu)) r.x = 0.0f;
+      if (!(mk & 0xFF00u)) r.y = 0.0f;
+      if (!(mk & 0xFF0000u)) r.z = 0.0f;
+      if (!(mk & 0xFF000000u)) r.w = 0.0f;
+    }
+    reinterpret_cast<float4*>(w)[i] = r;
+  }
+  // ragged tail (n % 4 tokens)
+  const int64_t tail = n - (n4 << 2);
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gt < tail) {
+    const int64_t j = (n4 << 2) + gt;
+    float r = tis_one(lt[j], lr[j], c_hi, c_lo, T);
+    if (mask && !mask[j]) r = 0.0f;
+    w[j] = r;
+  }
+}
+
+fx::Exp2Table make_table() {
+  fx::Exp2Table T;
+  for (int j = 0; j < 32; ++j) {
+    const double v = exp2(j / 32.0);
+    T.hi[j] = (float)v;
+    T.lo[j] = (float)(v - (double)T.hi[j]);
+  }
+  return T;
+}
+
+}  // namespace
+}  // namespace fp8rl
+
+using namespace fp8rl;
+
+extern "C" fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* logp_rollout,
+                                          const uint8_t* mask, int64_t n, float c_hi, float c_lo,
+                                          float* w, cudaStream_t stream) {
+  if (!logp_train || !logp_rollout || !w) return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (n < 0) return fail(FP8RL_ERR_INVALID_ARG, "n must be >= 0");
+  if (!(c_hi > 0.0f) || !std::isfinite(c_hi) || !(c_lo >= 0.0f) || !(c_lo <= c_hi))
+    return fail(FP8RL_ERR_INVALID_ARG, "need 0 <= c_lo <= c_hi, c_hi finite and > 0");
+  if (!aligned(logp_train, 16) || !aligned(logp_rollout, 16) || !aligned(w, 16) ||
+      (mask && !aligned(mask, 4)))
+    return fail(FP8RL_ERR_ALIGNMENT, "log-prob and weight arrays must be 16-byte aligned, mask 4-byte");
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  if (st != FP8RL_OK) return st;
+  if (n == 0) return ok();
+  static const fx::Exp2Table T = make_table();
+  const int64_t threads_needed = std::max<int64_t>((n + 3) / 4, 1);
+  int64_t ctas = (threads_needed + 255) / 256;
+  ctas = std::min<int64_t>(ctas, (int64_t)ds->sm_count * 8);
+  tis_kernel<<<(unsigned)ctas, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi, c_lo, w,
+                                                 T);
+  st = cuda_check(cudaGetLastError(), "tis_kernel launch");
+  return st == FP8RL_OK ? ok() : st;
+}

@@ -1,0 +1,188 @@
+/*
+ * fp8rl.h -- C ABI of the GB300 (sm_103a) FP8 rollout hot path.
+ *
+ * The operations are those of "FP8-RL: A Practical and Stable Low-Precision
+ * Stack for LLM Reinforcement Learning" (arXiv 2601.18150), as described by
+ * its long-form summary page (sections 3.4.1-3.4.4) and abstract:
+ *   - per-step blockwise re-quantization of BF16 policy weights into E4M3
+ *     with one FP32 scale per 128x128 block,
+ *   - per-token 1x128-group dynamic activation quantization,
+ *   - a blockwise-scaled FP8 W8A8 GEMM with FP32 accumulation and BF16
+ *     output, plus a grouped variant for MoE experts,
+ *   - FP8 E4M3 KV-cache quantization with per-head scales,
+ *   - token-level truncated importance-sampling (TIS) weights.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Numerics.  scale = fl32(amax / 448) (IEEE binary32 division), and a value
+ *   x is stored as code = E4M3(fl32(x / scale)): the binary32 quotient
+ *   rounded to nearest-even into E4M3 (OCP "e4m3fn": bias 7, max 448, no
+ *   infinities), saturating at +-448, keeping the sign of zero.  A block,
+ *   group or head whose amax is 0 gets scale 0 and codes +-0.  Results are
+ *   bit-identical to that definition for every finite input.
+ * BF16 inputs are raw bfloat16 bit patterns (2 bytes each); E4M3 codes are
+ *   bytes.  All sizes are in elements unless the name says bytes.
+ * Memory.  Every pointer argument is DEVICE memory on the current CUDA
+ *   device unless the comment says HOST.  The caller owns every buffer.  The
+ *   library owns one small per-device workspace (a status word and
+ *   calibration slots), allocated by the first call that needs it on that
+ *   device and kept until process exit; make that first call outside CUDA
+ *   graph capture.
+ * Streams.  Every compute call is asynchronous and stream-ordered on
+ *   `stream` (0 = legacy default stream); it returns after launching.
+ *   Argument errors are detected on the host before anything is launched.
+ * Errors.  Calls return fp8rl_status; on failure fp8rl_last_error() gives a
+ *   human-readable message (thread-local, valid until the next call on that
+ *   thread).  No call throws, aborts or traps.  Kernels never fault on
+ *   purpose: a device-side wait that exceeds its time limit sets a bit in
+ *   the device status word and the kernel returns early; read it with
+ *   fp8rl_device_status().
+ */
+#ifndef FP8RL_H_
+#define FP8RL_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8RL_VERSION 100
+
+typedef enum fp8rl_status {
+  FP8RL_OK = 0,
+  FP8RL_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad mode */
+  FP8RL_ERR_ALIGNMENT = 2,          /* pointer or leading dimension misaligned */
+  FP8RL_ERR_UNSUPPORTED_SHAPE = 3,  /* shape outside what a kernel supports */
+  FP8RL_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed */
+  FP8RL_ERR_TIMEOUT = 5,            /* a device-side wait hit its time limit */
+  FP8RL_ERR_UNSUPPORTED_DEVICE = 6  /* current device is not sm_103 */
+} fp8rl_status;
+
+typedef enum fp8rl_kv_mode {
+  FP8RL_KV_GIVEN = 0,      /* quantize with the caller's scales[heads] */
+  FP8RL_KV_CALIBRATE = 1   /* compute scales[h] = amax_h/448 from x, write them, quantize */
+} fp8rl_kv_mode;
+
+/* One tensor of a multi-tensor weight re-quantization (see
+ * fp8rl_quantize_weights_blockwise for the meaning of each field). */
+typedef struct fp8rl_wdesc {
+  const void* w;   /* BF16 [n, k], row stride ldw elements */
+  uint8_t* q;      /* E4M3 [n, k], row stride ldq bytes */
+  float* scales;   /* FP32 [ceil(n/128), ceil(k/128)], row-major */
+  int64_t n, k, ldw, ldq;
+} fp8rl_wdesc;
+
+/* Library version (FP8RL_VERSION of the build). */
+int32_t fp8rl_version(void);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* fp8rl_last_error(void);
+
+/* Blockwise weight re-quantization.
+ * Summary page section 3.4.1, equation W_hat_ij = round(W_ij / scale_ij) with
+ * scale_ij from the max-abs of the 128x128 block holding (i, j); section 3.4.2
+ * Phase 2 step 2 (runs every RL step on every quantized linear).
+ *   w       BF16 [n, k] row-major with row stride ldw (elements), 16-byte aligned
+ *   q       E4M3 codes [n, k], row stride ldq (bytes), 8-byte aligned
+ *   scales  FP32 [ceil(n/128), ceil(k/128)] row-major; scales[bi][bj] belongs to
+ *           rows [128 bi, 128 bi + 128) x cols [128 bj, 128 bj + 128)
+ * Edge blocks (n or k not a multiple of 128) take amax over their valid
+ * elements only.  Requires n, k >= 1, k % 8 == 0, ldw % 8 == 0, ldq % 8 == 0,
+ * ldw >= k, ldq >= k.  One read of w and one write of q. */
+fp8rl_status fp8rl_quantize_weights_blockwise(const void* w, int64_t n, int64_t k, int64_t ldw,
+                                              uint8_t* q, int64_t ldq, float* scales,
+                                              cudaStream_t stream);
+
+/* The same operation over `count` tensors in one pass (the per-step sync of
+ * a whole model; section 3.4.2 notes it is parallel across blocks and layers).
+ *   descs   HOST array of `count` descriptors (read during the call only);
+ *           each obeys the requirements above; tensors must not overlap.
+ * Tensors are processed in launches of up to 256 descriptors. */
+fp8rl_status fp8rl_quantize_weights_blockwise_multi(const fp8rl_wdesc* descs, int32_t count,
+                                                    cudaStream_t stream);
+
+/* Per-token 1x128-group activation quantization (dynamic quantization of
+ * section 3.4.1 "Static vs. Dynamic Quantization" and section 3.4.2 Phase 3;
+ * 1x128 tiles as in section 3.4.1).
+ *   a       BF16 [m, k], row stride lda (elements), 16-byte aligned
+ *   q       E4M3 codes [m, k] dense (row stride k bytes), 8-byte aligned
+ *   scales  FP32 [ceil(k/128), m]: GROUP-MAJOR, scales[g * m + r] is the scale
+ *           of row r, columns [128 g, 128 g + 128).  This is the layout the
+ *           GEMMs read (one contiguous vector of m-scales per k-block).
+ * Requires m, k >= 1, k % 8 == 0, lda % 8 == 0, lda >= k. */
+fp8rl_status fp8rl_quantize_act_groupwise(const void* a, int64_t m, int64_t k, int64_t lda,
+                                          uint8_t* q, float* scales, cudaStream_t stream);
+
+/* Blockwise-scaled W8A8 GEMM, Y = A W^T.
+ * Section 3.4.2 Phase 3 (FP8 x FP8 matmul on tensor cores, FP32 accumulation,
+ * BF16 result) with the scales of sections 3.4.1 (weights 128x128) and the
+ * activation groups above:
+ *   Y[i, j] = bf16( sum_kb sa[kb, i] * sw[j/128, kb] * sum_{k in kb} dec(qa[i,k]) dec(qw[j,k]) )
+ *   qa  E4M3 [m, k] dense;    sa  FP32 [k/128, m] (group-major, as above)
+ *   qw  E4M3 [n, k] dense;    sw  FP32 [ceil(n/128), k/128] row-major
+ *   y   BF16 [m, n], row stride ldy (elements)
+ * Requires m >= 0, n >= 16, k >= 128, k % 128 == 0, n % 16 == 0, ldy % 8 == 0,
+ * ldy >= n; qa, qw 16-byte aligned; y 16-byte aligned.  m = 0 is a no-op.
+ * Accuracy: FP32 accumulation of per-128-k partial sums, each promoted with
+ * its scale pair; one final BF16 rounding. */
+fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* qw,
+                                       const float* sw, int64_t m, int64_t n, int64_t k,
+                                       void* y, int64_t ldy, cudaStream_t stream);
+
+/* Grouped (MoE expert) variant: rows [offsets[e], offsets[e+1]) of A are the
+ * tokens routed to expert e (section 3.4.1 "MoE expert layers: fc1, fc2") and
+ * are multiplied by expert e's weights.
+ *   qa       E4M3 [m_total, k] dense;  sa FP32 [k/128, m_total] group-major
+ *   qw       E4M3 [e, n, k];           sw FP32 [e, n/128, k/128]
+ *   offsets  int32 [e + 1] DEVICE, non-decreasing, offsets[0] = 0,
+ *            offsets[e] <= m_total; read by the kernel (no host sync)
+ *   y        BF16 [m_total, n] dense; rows outside every segment are not written
+ * Requires 1 <= e <= 1024, n % 128 == 0, k % 128 == 0, alignment as above.
+ * Empty segments are allowed. */
+fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, const float* sa,
+                                               const uint8_t* qw, const float* sw,
+                                               const int32_t* offsets, int32_t num_experts,
+                                               int64_t m_total, int64_t n, int64_t k,
+                                               void* y, cudaStream_t stream);
+
+/* FP8 E4M3 KV-cache quantization with per-head scales (section 3.4.4: K and V
+ * stored as E4M3 with per-layer or per-head scales computed from the K/V the
+ * first rollout forward observes).  Call once for K and once for V.
+ *   x        BF16 [rows, heads, head_dim] dense (rows = sequences x tokens), 16-byte aligned
+ *   mode     FP8RL_KV_GIVEN: scales[heads] is an input;
+ *            FP8RL_KV_CALIBRATE: scales[h] = fl32(amax_h / 448) over all rows
+ *            and dims of head h is computed from x and written, then used
+ *   scales   FP32 [heads] (input or output per mode)
+ *   q        E4M3 [rows, heads, head_dim] dense, 8-byte aligned
+ * Requires head_dim % 8 == 0, heads * head_dim <= 2048, heads <= 256.
+ * CALIBRATE uses the library workspace: do not overlap two CALIBRATE calls on
+ * one device (different streams) -- they share the calibration slots. */
+fp8rl_status fp8rl_quantize_kv_fp8(const void* x, int64_t rows, int32_t heads, int32_t head_dim,
+                                   int32_t mode, float* scales, uint8_t* q, cudaStream_t stream);
+
+/* Token-level truncated importance-sampling weights (section 3.4.3):
+ *   w[i] = pi_theta / pi_fp8 = exp(logp_train[i] - logp_rollout[i]), truncated:
+ *   d = fl32(logp_train - logp_rollout); e = RN32(e^d), the correctly rounded
+ *   binary32 exponential; w = min(e, c_hi), then max(w, c_lo) if c_lo > 0;
+ *   NaN stays NaN; w = 0 where mask[i] == 0.
+ *   logp_train, logp_rollout  FP32 [n], 16-byte aligned
+ *   mask     uint8 [n] or NULL (all tokens valid)
+ *   c_hi     truncation C (2 in the pages' experiments), finite, > 0
+ *   c_lo     0 for the one-sided min(w, C); 1/C for the two-sided [1/C, C]
+ *   w        FP32 [n], 16-byte aligned */
+fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* logp_rollout,
+                               const uint8_t* mask, int64_t n, float c_hi, float c_lo, float* w,
+                               cudaStream_t stream);
+
+/* Synchronizes the device and returns FP8RL_ERR_TIMEOUT if any kernel since
+ * the last clear hit a device-side wait limit (FP8RL_OK otherwise); clears
+ * the word when clear != 0.  device = CUDA ordinal. */
+fp8rl_status fp8rl_device_status(int32_t device, int32_t clear);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* FP8RL_H_ */

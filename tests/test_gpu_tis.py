@@ -1,0 +1,78 @@
+"""GPU parity of the truncated importance weights: bit-exact against the
+oracle on the pages' workloads, with masks, both clip modes, ragged sizes,
+special values, and exhaustively over every binary32 log-ratio."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_precision_rollout_gb300 as fp8rl
+import oracle
+from fp8_precision_rollout_gb300 import workloads
+from gpu_helpers import Canary, device, np_f32_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(lt, lr, dev, mask=None, c_hi=2.0, c_lo=0.0):
+    n = lt.numel()
+    wc = Canary(max(n, 1), torch.float32, dev)
+    w = wc.view[:n]
+    fp8rl.tis_weights(lt.to(dev), lr.to(dev), None if mask is None else mask.to(dev), c_hi, c_lo,
+                      w=w)
+    torch.cuda.synchronize()
+    wc.check()
+    ref = oracle.tis_weights(lt.numpy(), lr.numpy(),
+                             None if mask is None else mask.numpy(), c_hi, c_lo)
+    got = w.cpu().numpy()
+    same = (got.view(np.uint32) == ref.view(np.uint32)) | (np.isnan(got) & np.isnan(ref))
+    assert same.all(), "first mismatch at %s" % np.argwhere(~same)[:5].ravel()
+
+
+def test_tiny_workload():
+    dev = device()
+    lt, lr = workloads.tis_logprobs(4096, seed=0)
+    _case(lt, lr, dev)
+    _case(lt, lr, dev, c_lo=0.5)
+    mask = (torch.arange(4096) % 7 != 3).to(torch.uint8)
+    _case(lt, lr, dev, mask=mask)
+
+
+def test_long_context_student_t_workload():
+    dev = device()
+    lt, lr = workloads.tis_logprobs(64 * 20480, seed=5, kind="student_t")
+    _case(lt, lr, dev)
+    _case(lt, lr, dev, c_hi=2.0, c_lo=0.5)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 4097, 1023])
+def test_ragged_sizes(n):
+    dev = device()
+    lt, lr = workloads.tis_logprobs(n, seed=n)
+    mask = (torch.arange(n) % 2).to(torch.uint8)
+    _case(lt, lr, dev)
+    _case(lt, lr, dev, mask=mask)
+
+
+def test_special_values():
+    dev = device()
+    v = torch.tensor([0.0, -0.0, float("nan"), float("inf"), -float("inf"), 88.0, 89.0, -87.0,
+                      -104.0, -103.9, -150.0, 1e-30, -2.0 ** -25, 0.6931472, 0.69314712],
+                     dtype=torch.float32)
+    _case(v, torch.zeros_like(v), dev)
+    _case(torch.zeros_like(v), v, dev, c_hi=1e30)
+
+
+def test_every_binary32_log_ratio():
+    """lt = every float32 bit pattern, lr = 0, so d = lt exactly; C = 3e38
+    (no truncation) so the raw correctly rounded exponential is compared."""
+    dev = device()
+    chunk = 1 << 28
+    for start in range(0, 1 << 32, chunk):
+        bits = torch.arange(start, start + chunk, dtype=torch.int64, device=dev).to(torch.int32)
+        lt = bits.view(torch.float32)
+        w = fp8rl.tis_weights(lt, torch.zeros_like(lt), None, 3e38, 0.0)
+        ref = oracle.tis_weights(lt.cpu().numpy(), np.zeros(chunk, np.float32), None, 3e38, 0.0)
+        got = w.cpu().numpy()
+        same = (got.view(np.uint32) == ref.view(np.uint32)) | (np.isnan(got) & np.isnan(ref))
+        assert same.all(), "chunk %x: %d mismatches" % (start, (~same).sum())
+        del bits, lt, w
