@@ -181,7 +181,7 @@ class Workload:
 
         mark("a1_start")
         fp8rl.quantize_weights_blockwise_multi(self.w, self.q, self.s)
-        launches += (len(self.w) + 255) // 256
+        launches += (len(self.w) + 159) // 160
         mark("a1_end")
         for g in self.gemms:
             key = "gemm_%s_m%d" % (g["name"], g["m"])

@@ -22,8 +22,9 @@
 //    arithmetic", ACM TOMS 15(2), 1989) with 32 table entries and a degree-6
 //    Taylor polynomial, accurate to ~2^-44 relative; inputs whose result lies
 //    within 2^-40 of a binary32 rounding boundary, or outside |d| <= 87, are
-//    recomputed with a double-double Taylor series (~2^-99) whose rounding is
-//    then exact.
+//    recomputed in double-double arithmetic (argument reduced by ln 2 and
+//    scaled by 2^-8, degree-11 Taylor series, eight squarings; ~2^-95), whose
+//    rounding is then exact.
 #pragma once
 
 #include <stdint.h>
@@ -31,8 +32,10 @@
 
 #if defined(__CUDACC__)
 #define FP8RL_HD __host__ __device__ __forceinline__
+#define FP8RL_HD_OUTLINE static __host__ __device__ __noinline__
 #else
 #define FP8RL_HD inline
+#define FP8RL_HD_OUTLINE inline
 #endif
 
 namespace fp8rl {
@@ -97,13 +100,14 @@ FP8RL_HD ScaleDiv make_scale_div(float s) {
 
 // fl32(x / s) when mode == 1, |x / s| < 2^127 and |x| >= 2^-71; for smaller
 // |x| the result is within a few ulps of a quotient below 2^-11 (guarded
-// variant below for arbitrary caller scales).  The final copysign restores the sign
-// of a zero x, which the correction step would otherwise turn into +0.
+// variant below for arbitrary caller scales).  The residual is formed as
+// q0*s - x and applied with -y: the same value as Markstein's
+// q0 + (x - q0*s)*y for every non-zero x, and for x = -0 it yields -0 (the
+// form with x - q0*s would return +0), so the sign of zero needs no fix-up.
 FP8RL_HD float markstein_quotient(float x, float s, float y) {
-  float q0 = fmul(x, y);
-  float r = ffma(-q0, s, x);
-  float q1 = ffma(r, y, q0);
-  return copysignf(q1, x);
+  const float q0 = fmul(x, y);
+  const float rp = ffma(q0, s, -x);
+  return ffma(rp, -y, q0);
 }
 
 // The element map's binary32 quotient under a prepared scale.  kGuard adds
@@ -126,10 +130,14 @@ FP8RL_HD float scaled_quotient(float x, const ScaleDiv& d) {
 
 // ---------------------------------------------- correctly rounded e^d ------
 
-// 2^(j/32), j = 0..31, as float-float pairs (hi + lo), built on the host.
+// Tables of the exponential, built on the host by make_exp_tables():
+// 2^(j/32), j = 0..31, as float-float pairs, and 1/i, i = 1..11, as
+// double-double pairs.
 struct Exp2Table {
   float hi[32];
   float lo[32];
+  double inv_hi[12];
+  double inv_lo[12];
 };
 
 FP8RL_HD void two_sum(float a, float b, float& s, float& e) {
@@ -217,12 +225,6 @@ FP8RL_HD dd dd_mul(dd a, dd b) {
   e = dadd(e, dadd(dmul(a.hi, b.lo), dmul(a.lo, b.hi)));
   return dd_fast(p, e);
 }
-FP8RL_HD dd dd_div_small(dd a, double i) {   // i a small positive integer
-  double q1 = ddiv(a.hi, i);
-  double rem = dfma(-q1, i, a.hi);             // exact
-  double q2 = ddiv(dadd(rem, a.lo), i);
-  return dd_fast(q1, q2);
-}
 FP8RL_HD dd dd_add_one(dd a) {
   dd s = dd_two_sum(1.0, a.hi);
   return dd_fast(s.hi, dadd(s.lo, a.lo));
@@ -243,8 +245,9 @@ FP8RL_HD float dd_round_to_float(double H, double L) {
   return f;
 }
 
-// Slow path: any binary32 d.
-FP8RL_HD float exp_rn32_slow(float d) {
+// Slow path: any binary32 d.  Kept out of line: it runs for a few lanes in
+// ten thousand, and inlining it at every call site would bloat the fast path.
+FP8RL_HD_OUTLINE float exp_rn32_slow(float d, const Exp2Table& T) {
   if (d != d) return d;
   if (d > 89.0f) return INFINITY;      // e^89 > 2^128: rounds to +inf
   if (d < -104.0f) return 0.0f;        // e^-104 < 2^-150: rounds to +0
@@ -256,13 +259,16 @@ FP8RL_HD float exp_rn32_slow(float d) {
   double p1e = dfma(k, kLn2Hi, -p1);
   dd r = dd_two_sum(x, -p1);
   r = dd_fast(r.hi, dsub(dsub(r.lo, p1e), dmul(k, kLn2Lo)));
-  // e^r, |r| <= ~0.35: Horner 1 + r/i (1 + r/(i+1)(...)) down from i = 27
+  r.hi = dmul(r.hi, 0x1p-8);                      // exact scaling: |r| <= ~0.0014
+  r.lo = dmul(r.lo, 0x1p-8);
+  // e^r = 1 + r/1 (1 + r/2 (1 + ... (1 + r/11))), truncation < 2^-130
   dd p{1.0, 0.0};
-  for (int i = 27; i >= 1; --i) {
+  for (int i = 11; i >= 1; --i) {
     p = dd_mul(p, r);
-    p = dd_div_small(p, (double)i);
+    p = dd_mul(p, dd{T.inv_hi[i], T.inv_lo[i]});
     p = dd_add_one(p);
   }
+  for (int i = 0; i < 8; ++i) p = dd_mul(p, p);   // (e^(r/256))^256
   int ki = (int)k;
   return dd_round_to_float(ldexp(p.hi, ki), ldexp(p.lo, ki));
 }
@@ -270,7 +276,26 @@ FP8RL_HD float exp_rn32_slow(float d) {
 FP8RL_HD float exp_rn32(float d, const Exp2Table& T) {
   float e;
   if (exp_rn32_fast(d, T, &e)) return e;
-  return exp_rn32_slow(d);
+  return exp_rn32_slow(d, T);
+}
+
+// Host-side construction of the tables (C library exp2 in double, good to
+// ~2^-52; the float-float pairs keep 48 bits, the fast path's error budget
+// allows 2^-44).  1/i is split exactly: lo = RN((1 - hi*i) / i) with the
+// residual 1 - hi*i formed exactly by an FMA.
+inline Exp2Table make_exp_tables() {
+  Exp2Table T;
+  for (int j = 0; j < 32; ++j) {
+    const double v = exp2(j / 32.0);
+    T.hi[j] = (float)v;
+    T.lo[j] = (float)(v - (double)T.hi[j]);
+  }
+  T.inv_hi[0] = T.inv_lo[0] = 0.0;
+  for (int i = 1; i < 12; ++i) {
+    T.inv_hi[i] = 1.0 / i;
+    T.inv_lo[i] = fma(-T.inv_hi[i], (double)i, 1.0) / i;
+  }
+  return T;
 }
 
 }  // namespace fx

@@ -13,7 +13,8 @@
 // the hardware's block-scaled MMA (power-of-two UE8M0 scales per 32 K).  Each
 // 128-wide k-block is therefore one MMA group writing a fresh FP32 partial
 // P_kb into tensor memory; epilogue warps read it back (tcgen05.ld, 16 columns at a time), multiply
-// by sa*sw and add it into FP32 register accumulators.
+// by sa*sw and add it into FP32 register accumulators (packed FP32x2 FMAs;
+// the scales of k-block kb+1 are fetched while kb is promoted).
 //
 // Kernel shape (one CTA per SM, persistent over output tiles):
 //   tile 128 (M) x 256 (N), k-block 128; 4-stage TMA ring of 48 KB stages
@@ -27,14 +28,13 @@
 //   k-block kb+1 overlaps the promotion of kb.
 // Every wait on an mbarrier is bounded (1 s); on expiry the kernel records it
 // in the library's device status word, drains what it issued and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
 #include <mutex>
 
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace fp8rl {
 namespace {
@@ -46,7 +46,6 @@ constexpr int kBStage = BN * BK;                 // 32 KB
 constexpr int kStageBytes = kAStage + kBStage;   // 48 KB
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr int kMGroup = 16;                      // m-tiles per raster band (L2 reuse)
 
 // tcgen05 instruction descriptor, kind::f8f6f4: D = F32 (bits 4-5 = 1),
@@ -82,113 +81,19 @@ struct GemmArgs {
   uint32_t* status;        // library status word
 };
 
-// ------------------------------------------------------------ PTX wrappers --
+using namespace ptx;
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t a) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded wait for the phase of parity `parity`.  false: the CTA is aborting
-// (this wait timed out, or another role's did).
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile uint32_t* abort_flag,
-                                       uint32_t* status, uint32_t site) {
-  if (mbar_try(a, parity)) return true;
-  const uint64_t t0 = gtimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try(a, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (gtimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1u;
-        atomicOr(status, kStatusGemmTimeout);
-        atomicExch(status + 1, site);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t mbar,
-                                            int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// 64-bit shared-memory matrix descriptor, K-major operand with 128-byte
-// swizzle: start address >> 4 (bits 0-13), leading offset 1 (unused for this
-// layout), stride between 8-row groups 1024 B >> 4 (bits 32-45), descriptor
-// version 1 (bits 46-47), base offset 0, layout SWIZZLE_128B = 2 (bits 61-63).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t mbar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// acc0 += p0 * f, acc1 += p1 * f as one packed FP32x2 FMA (each lane an IEEE
+// round-to-nearest FMA, the same result as two fmaf calls).
+__device__ __forceinline__ void ffma2(float& acc0, float& acc1, uint32_t p0, uint32_t p1, float f) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %4};\n\t"
+      "mov.b64 rc, {%0, %1};\n\t"
+      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(p0), "r"(p1), "f"(f));
 }
 
 // ---------------------------------------------------------- tile schedule --
@@ -314,16 +219,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     st->abort_flag = 0;
     if (!kGrouped) st->total_tiles = g.num_m * g.num_n;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_fence_init();
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&st->tmem_base)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tmem_alloc(smem_u32(&st->tmem_base), kTmemCols);
   }
   if (kGrouped) build_expert_schedule(g, st);
   tc_fence_before();
@@ -360,8 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
       for (uint32_t j = 1; j <= n; ++j) {
         const uint32_t i2 = it - j;
-        volatile uint32_t never = 0;
-        mbar_wait(smem_u32(&st->full[i2 % STAGES]), (i2 / STAGES) & 1u, &never, g.status, 9);
+        mbar_drain(smem_u32(&st->full[i2 % STAGES]), (i2 / STAGES) & 1u, g.status, 9);
       }
     }
     __syncwarp();
@@ -389,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = smem_u32(sB + s * kBStage);
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk)
-            mma_f8(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kk > 0 ? 1u : 0u);
+            mma_f8(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc, kk > 0 ? 1u : 0u);
           mma_commit(smem_u32(&st->empty[s]));
           mma_commit(smem_u32(&st->tfull[buf]));
         }
@@ -399,8 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && it > 0) {
       // the last stage release must have landed before the CTA exits
       const uint32_t i2 = it - 1;
-      volatile uint32_t never = 0;
-      mbar_wait(smem_u32(&st->empty[i2 % STAGES]), (i2 / STAGES) & 1u, &never, g.status, 8);
+      mbar_drain(smem_u32(&st->empty[i2 % STAGES]), (i2 / STAGES) & 1u, g.status, 8);
     }
     __syncwarp();
   } else {
@@ -420,12 +319,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      // scales of the next k-block are loaded one iteration ahead so their
+      // latency hides behind the current promotion
+      float sa_next = row_ok ? __ldg(g.sa + row) : 0.0f;
+      float sw_next = nb_ok ? __ldg(swp) : 0.0f;
       for (int kb = 0; kb < KB; ++kb, ++kit) {
         const int buf = kit & 1;
         const uint32_t u = kit >> 1;
-        const float sav = row_ok ? __ldg(g.sa + (int64_t)kb * g.M + row) : 0.0f;
-        const float swv = nb_ok ? __ldg(swp + kb) : 0.0f;
-        const float f = __fmul_rn(sav, swv);
+        const float f = __fmul_rn(sa_next, sw_next);
+        if (kb + 1 < KB) {
+          sa_next = row_ok ? __ldg(g.sa + (int64_t)(kb + 1) * g.M + row) : 0.0f;
+          sw_next = nb_ok ? __ldg(swp + kb + 1) : 0.0f;
+        }
         bool okw = mbar_wait(smem_u32(&st->tfull[buf]), u & 1u, abort_flag, g.status, 4);
         okw = __all_sync(0xFFFFFFFFu, okw);
         if (!okw) { alive = false; break; }
@@ -442,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&st->tempty[buf]));
           }
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            acc[c * 16 + j] = __fmaf_rn(__uint_as_float(p[j]), f, acc[c * 16 + j]);
+          for (int j = 0; j < 16; j += 2)
+            ffma2(acc[c * 16 + j], acc[c * 16 + j + 1], p[j], p[j + 1], f);
         }
       }
       if (!alive) break;
@@ -473,44 +378,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTmemCols)
-                 : "memory");
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
 // ------------------------------------------------------------------- host --
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // 2-D uint8 map over a row-major [rows, inner] matrix, box [box_rows, 128],
-// 128-byte swizzle (the layout the UMMA descriptors above describe).
+// 128-byte swizzle (the layout the UMMA descriptors describe).
 fp8rl_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
                       uint32_t box_rows, const char* what) {
-  auto fn = encode_fn();
-  if (!fn) return fail(FP8RL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner};
-  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(FP8RL_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what, (int)r);
-  return FP8RL_OK;
+  return encode_tiled_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner, rows, inner, BK, box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B, what);
 }
 
 template <bool kGrouped>

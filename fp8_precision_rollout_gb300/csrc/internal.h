@@ -1,6 +1,7 @@
 // internal.h -- host-side plumbing shared by the fp8rl translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,8 +33,15 @@ fp8rl_status device_state(DeviceState** out);
 
 // Device status word bits.
 enum : uint32_t {
-  kStatusGemmTimeout = 1u << 0,
+  kStatusTimeout = 1u << 0,   // a pipelined kernel gave up on an mbarrier wait
 };
+
+// Encodes a 2-D tiled TMA descriptor over a row-major [rows, inner] matrix of
+// `dtype` elements with row pitch `row_bytes`; box [box_rows, box_inner].
+fp8rl_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                             uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                             uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle,
+                             const char* what);
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 

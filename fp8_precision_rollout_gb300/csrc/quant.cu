@@ -20,6 +20,7 @@
 
 #include "fp_exact.cuh"
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace fp8rl {
 namespace {
@@ -72,7 +73,7 @@ __device__ __forceinline__ uint32_t quant2(uint32_t w, const ScaleDiv& sd) {
   return cvt_e4m3x2(scaled_quotient<kGuard>(x0, sd), scaled_quotient<kGuard>(x1, sd));
 }
 
-// 8 bf16 -> 8 codes packed in a uint2
+// 8 bf16 -> 8 codes packed in a uint2 (any prepared scale)
 template <bool kGuard>
 __device__ __forceinline__ uint2 quant8(const uint4& v, const ScaleDiv& sd) {
   uint2 r;
@@ -81,77 +82,185 @@ __device__ __forceinline__ uint2 quant8(const uint4& v, const ScaleDiv& sd) {
   return r;
 }
 
+// The same for a scale known to be in the Markstein range (mode 1), with no
+// per-element branch; kGuard as in scaled_quotient.
+template <bool kGuard>
+__device__ __forceinline__ float fast_quotient(float x, float s, float y) {
+  float q = fx::markstein_quotient(x, s, y);
+  if (kGuard) {
+    const float q0 = __fmul_rn(x, y);
+    q = fabsf(q0) < 1024.0f ? q : q0;
+  }
+  return q;
+}
+template <bool kGuard>
+__device__ __forceinline__ uint32_t quant2_fast(uint32_t w, float s, float y) {
+  return cvt_e4m3x2(fast_quotient<kGuard>(__uint_as_float(w << 16), s, y),
+                    fast_quotient<kGuard>(__uint_as_float(w & 0xFFFF0000u), s, y));
+}
+template <bool kGuard>
+__device__ __forceinline__ uint2 quant8_fast(const uint4& v, float s, float y) {
+  uint2 r;
+  r.x = quant2_fast<kGuard>(v.x, s, y) | (quant2_fast<kGuard>(v.y, s, y) << 16);
+  r.y = quant2_fast<kGuard>(v.z, s, y) | (quant2_fast<kGuard>(v.w, s, y) << 16);
+  return r;
+}
+
+// Dispatch once per scale: the common (mode 1) path has no element branch.
+template <bool kGuard>
+__device__ __forceinline__ uint2 quant8_any(const uint4& v, const ScaleDiv& sd) {
+  return sd.mode == 1 ? quant8_fast<kGuard>(v, sd.s, sd.y) : quant8<kGuard>(v, sd);
+}
+
 __device__ __forceinline__ float warp_max(float v, int width) {
   for (int o = width >> 1; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
 
 // -------------------------------------------------- 128x128 weight blocks --
+//
+// Persistent, TMA-fed: each CTA walks blocks blockIdx.x, +gridDim.x, ... of
+// all tensors of the launch.  A producer warp streams each 128x128 BF16 block
+// (32 KB) into a 2-stage shared-memory ring with one 2-D TMA load; eight
+// consumer warps copy the block to registers, release the stage, reduce the
+// block max (warp shuffles + a named barrier), and write the codes with 8-byte
+// stores.  Loads of the next blocks stay in flight across each block's
+// max -> quantize dependency; three CTAs per SM keep ~192 KB in flight.  Edge
+// blocks are zero-filled by TMA outside the tensor, which leaves the max of
+// the valid elements unchanged; stores are masked to the valid region.
 
-constexpr int kMaxDescs = 256;
+constexpr int kWQMaxDescs = 160;
+constexpr int kWQStages = 2;
+constexpr int kWQBlockBytes = 128 * 128 * 2;
+constexpr int kWQConsumerThreads = 256;
+constexpr int kWQThreads = kWQConsumerThreads + 32;
 
 struct WQDesc {
-  const uint16_t* w;
   uint8_t* q;
   float* scales;
-  int64_t n, k, ldw, ldq;
-  int32_t kb;      // ceil(k/128)
-  int32_t pad;
+  int64_t ldq;
+  int32_t n, k, kb, pad;
 };
 
 struct WQParams {
+  CUtensorMap map[kWQMaxDescs];     // BF16 [n, k], row pitch ldw*2, box 128 x 128, no swizzle
+  WQDesc d[kWQMaxDescs];
+  int32_t start[kWQMaxDescs + 1];   // first block id of each tensor; start[count] = total
   int32_t count;
-  int32_t start[kMaxDescs + 1];   // first block id of each tensor; start[count] = total
-  WQDesc d[kMaxDescs];
+  int32_t total;
+  uint32_t* status;
 };
 
-// One CTA of 256 threads per 128x128 block.  Warp w, half-warp h handles rows
-// 2w + h + 16i (i = 0..7); lane c of the half-warp the 16-byte column chunk c.
-// The block stays in registers between the max and the quantization: one HBM
-// read and one write per element.
-__global__ void __launch_bounds__(256) wquant_kernel(const __grid_constant__ WQParams p) {
-  const int b = blockIdx.x;
+struct WQShared {
+  uint64_t full[kWQStages];
+  uint64_t empty[kWQStages];
+  float red[2][8];
+  uint32_t abort_flag;
+};
+
+constexpr size_t kWQSmem = 1024 + (size_t)kWQStages * kWQBlockBytes + sizeof(WQShared);
+
+__device__ __forceinline__ int wq_find(const WQParams& p, int b) {
   int lo = 0, hi = p.count - 1;
   while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
+    const int mid = (lo + hi + 1) >> 1;
     if (p.start[mid] <= b) lo = mid; else hi = mid - 1;
   }
-  const WQDesc& d = p.d[lo];
-  const int local = b - p.start[lo];
-  const int bi = local / d.kb, bj = local - (local / d.kb) * d.kb;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t r0 = (int64_t)bi * 128 + warp * 2 + (lane >> 4);
-  const int64_t col = (int64_t)bj * 128 + (lane & 15) * 8;
-  const bool full = ((int64_t)bi * 128 + 128 <= d.n) && ((int64_t)bj * 128 + 128 <= d.k);
-  const bool col_ok = col < d.k;
+  return lo;
+}
 
-  uint4 v[8];
-  uint32_t m2 = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t r = r0 + 16 * i;
-    if (full || (col_ok && r < d.n)) {
-      v[i] = ld_stream(d.w + r * d.ldw + col);
-    } else {
-      v[i] = make_uint4(0, 0, 0, 0);
+__global__ void __launch_bounds__(kWQThreads, 3) wquant_kernel(const __grid_constant__ WQParams p) {
+  using namespace ptx;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  WQShared* sh = reinterpret_cast<WQShared*>(smem + kWQStages * kWQBlockBytes);
+  volatile uint32_t* abort_flag = &sh->abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kWQStages; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), kWQConsumerThreads / 32);
     }
-    m2 = absmax8(m2, v[i]);
+    sh->abort_flag = 0;
+    mbar_fence_init();
   }
-  float amax = warp_max(bf16x2_maxf(m2), 32);
-  __shared__ float red[8];
-  if (lane == 0) red[warp] = amax;
   __syncthreads();
-  amax = red[0];
+
+  if (warp == kWQConsumerThreads / 32) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      uint32_t i = 0;
+      for (int b = blockIdx.x; b < p.total; b += gridDim.x, ++i) {
+        const int t = wq_find(p, b);
+        const WQDesc& d = p.d[t];
+        const int local = b - p.start[t];
+        const int bi = local / d.kb, bj = local - (local / d.kb) * d.kb;
+        const int s = i % kWQStages;
+        const uint32_t ph = (i / kWQStages) & 1u;
+        if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.status, 21)) {
+          // let the loads already issued land before the CTA exits
+          const uint32_t n = i < (uint32_t)kWQStages ? i : (uint32_t)kWQStages;
+          for (uint32_t j = 1; j <= n; ++j)
+            mbar_drain(smem_u32(&sh->full[(i - j) % kWQStages]), ((i - j) / kWQStages) & 1u,
+                       p.status, 22);
+          break;
+        }
+        const uint32_t fb = smem_u32(&sh->full[s]);
+        mbar_expect_tx(fb, kWQBlockBytes);
+        tma_load_2d(smem_u32(smem + s * kWQBlockBytes), &p.map[t], fb, bj * 128, bi * 128);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- consumers --
+    uint32_t i = 0;
+    for (int b = blockIdx.x; b < p.total; b += gridDim.x, ++i) {
+      const int t = wq_find(p, b);
+      const WQDesc& d = p.d[t];
+      const int local = b - p.start[t];
+      const int bi = local / d.kb, bj = local - (local / d.kb) * d.kb;
+      const int s = i % kWQStages;
+      const uint32_t ph = (i / kWQStages) & 1u;
+      bool okw = mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.status, 23);
+      okw = __all_sync(0xFFFFFFFFu, okw);
+      if (!okw) break;
+      // chunk c = tid + 256 j of the block: row c / 16, columns (c % 16) * 8 .. + 8
+      const uint4* stage = reinterpret_cast<const uint4*>(smem + s * kWQBlockBytes);
+      uint4 v[8];
 #pragma unroll
-  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-  const float s = fx::fdiv(amax, 448.0f);
-  if (tid == 0) d.scales[(int64_t)bi * d.kb + bj] = s;
-  const ScaleDiv sd = make_scale_div(s);
+      for (int j = 0; j < 8; ++j) v[j] = stage[tid + kWQConsumerThreads * j];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->empty[s]));
+      uint32_t m2 = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t r = r0 + 16 * i;
-    if (full || (col_ok && r < d.n)) {
-      *reinterpret_cast<uint2*>(d.q + r * d.ldq + col) = quant8<false>(v[i], sd);
+      for (int j = 0; j < 8; ++j) m2 = absmax8(m2, v[j]);
+      float amax = warp_max(bf16x2_maxf(m2), 32);
+      if (lane == 0) sh->red[i & 1][warp] = amax;
+      named_bar(1, kWQConsumerThreads);
+      amax = sh->red[i & 1][0];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, sh->red[i & 1][w]);
+      const float sc = fx::fdiv(amax, 448.0f);
+      if (tid == 0) d.scales[(int64_t)bi * d.kb + bj] = sc;
+      const ScaleDiv sd = make_scale_div(sc);
+      const int col = bj * 128 + (tid & 15) * 8;
+      const int row0 = bi * 128 + (tid >> 4);
+      const bool full = (bi * 128 + 128 <= d.n) && (bj * 128 + 128 <= d.k);
+      if (full && sd.mode == 1) {
+        uint8_t* qp = d.q + (int64_t)row0 * d.ldq + col;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint2*>(qp + (int64_t)(16 * j) * d.ldq) =
+              quant8_fast<false>(v[j], sd.s, sd.y);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = row0 + 16 * j;
+          if (r < d.n && col < d.k)
+            *reinterpret_cast<uint2*>(d.q + (int64_t)r * d.ldq + col) = quant8<false>(v[j], sd);
+        }
+      }
     }
   }
 }
@@ -167,9 +276,8 @@ fp8rl_status check_wdesc(const fp8rl_wdesc& d, int idx) {
     return fail(FP8RL_ERR_ALIGNMENT, "weight tensor %d: k, ldw and ldq must be multiples of 8", idx);
   if (!aligned(d.w, 16) || !aligned(d.q, 8) || !aligned(d.scales, 4))
     return fail(FP8RL_ERR_ALIGNMENT, "weight tensor %d: w must be 16-byte, q 8-byte aligned", idx);
-  int64_t blocks = ((d.n + 127) / 128) * ((d.k + 127) / 128);
-  if (blocks > (int64_t)1 << 30)
-    return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "weight tensor %d: too many blocks", idx);
+  if (d.n > INT32_MAX / 2 || d.k > INT32_MAX / 2 || d.ldq > INT32_MAX)
+    return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "weight tensor %d: dimension too large", idx);
   return FP8RL_OK;
 }
 
@@ -209,7 +317,7 @@ __global__ void __launch_bounds__(256) aquant_kernel(const uint16_t* __restrict_
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t col = gcol + (slot + 4 * i) * 8;
-      if (g < kb && col < k) *reinterpret_cast<uint2*>(qrow + col) = quant8<false>(v[i], sd);
+      if (g < kb && col < k) *reinterpret_cast<uint2*>(qrow + col) = quant8_any<false>(v[i], sd);
     }
   }
 }
@@ -274,14 +382,14 @@ __global__ void __launch_bounds__(256) kv_quant_kernel(const uint16_t* __restric
     uint4 a1 = ld_stream(x + (r + stride) * row_elems + v * 8);
     uint4 a2 = ld_stream(x + (r + 2 * stride) * row_elems + v * 8);
     uint4 a3 = ld_stream(x + (r + 3 * stride) * row_elems + v * 8);
-    *reinterpret_cast<uint2*>(q + r * row_elems + v * 8) = quant8<!kCalibrated>(a0, sd);
-    *reinterpret_cast<uint2*>(q + (r + stride) * row_elems + v * 8) = quant8<!kCalibrated>(a1, sd);
-    *reinterpret_cast<uint2*>(q + (r + 2 * stride) * row_elems + v * 8) = quant8<!kCalibrated>(a2, sd);
-    *reinterpret_cast<uint2*>(q + (r + 3 * stride) * row_elems + v * 8) = quant8<!kCalibrated>(a3, sd);
+    *reinterpret_cast<uint2*>(q + r * row_elems + v * 8) = quant8_any<!kCalibrated>(a0, sd);
+    *reinterpret_cast<uint2*>(q + (r + stride) * row_elems + v * 8) = quant8_any<!kCalibrated>(a1, sd);
+    *reinterpret_cast<uint2*>(q + (r + 2 * stride) * row_elems + v * 8) = quant8_any<!kCalibrated>(a2, sd);
+    *reinterpret_cast<uint2*>(q + (r + 3 * stride) * row_elems + v * 8) = quant8_any<!kCalibrated>(a3, sd);
   }
   for (; r < rows; r += stride)
     *reinterpret_cast<uint2*>(q + r * row_elems + v * 8) =
-        quant8<!kCalibrated>(ld_stream(x + r * row_elems + v * 8), sd);
+        quant8_any<!kCalibrated>(ld_stream(x + r * row_elems + v * 8), sd);
 }
 
 int grid_for(int64_t work_ctas, const DeviceState* ds, int per_sm) {
@@ -307,26 +415,45 @@ extern "C" fp8rl_status fp8rl_quantize_weights_blockwise_multi(const fp8rl_wdesc
   DeviceState* ds = nullptr;
   fp8rl_status st = device_state(&ds);
   if (st != FP8RL_OK) return st;
-  static WQParams p;   // large: keep off the stack; guarded by the launch sequence below
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
-  for (int base = 0; base < count; base += kMaxDescs) {
-    const int c = std::min(kMaxDescs, count - base);
+  static bool attr_done[64] = {false};
+  if (ds->device < 64 && !attr_done[ds->device]) {
+    st = cuda_check(cudaFuncSetAttribute(wquant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kWQSmem),
+                    "cudaFuncSetAttribute(wquant)");
+    if (st != FP8RL_OK) return st;
+    attr_done[ds->device] = true;
+  }
+  static WQParams p;   // ~25 KB of kernel parameters, filled per launch under the lock
+  for (int base = 0; base < count; base += kWQMaxDescs) {
+    const int c = std::min(kWQMaxDescs, count - base);
     std::memset(&p, 0, sizeof(p));
     p.count = c;
+    p.status = ds->status;
     int64_t total = 0;
     for (int i = 0; i < c; ++i) {
       const fp8rl_wdesc& d = descs[base + i];
       const int64_t kb = (d.k + 127) / 128;
       p.start[i] = (int32_t)total;
-      p.d[i] = WQDesc{reinterpret_cast<const uint16_t*>(d.w), d.q, d.scales, d.n, d.k,
-                      d.ldw, d.ldq, (int32_t)kb, 0};
+      st = encode_tiled_2d(&p.map[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.w, (uint64_t)d.k,
+                           (uint64_t)d.n, (uint64_t)d.ldw * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           "weight");
+      if (st != FP8RL_OK) return st;
+      p.d[i].q = d.q;
+      p.d[i].scales = d.scales;
+      p.d[i].ldq = d.ldq;
+      p.d[i].n = (int32_t)d.n;
+      p.d[i].k = (int32_t)d.k;
+      p.d[i].kb = (int32_t)kb;
       total += ((d.n + 127) / 128) * kb;
       if (total > INT32_MAX)
         return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "more than 2^31 blocks in one launch");
     }
     p.start[c] = (int32_t)total;
-    wquant_kernel<<<(unsigned)total, 256, 0, stream>>>(p);
+    p.total = (int32_t)total;
+    const int grid = (int)std::min<int64_t>(total, (int64_t)ds->sm_count * 3);
+    wquant_kernel<<<grid, kWQThreads, kWQSmem, stream>>>(p);
     st = cuda_check(cudaGetLastError(), "wquant_kernel launch");
     if (st != FP8RL_OK) return st;
   }

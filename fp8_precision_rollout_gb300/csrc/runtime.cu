@@ -1,4 +1,6 @@
 // runtime.cu -- error reporting, per-device state and workspace, status word.
+#include <cudaTypedefs.h>
+
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -68,6 +70,40 @@ fp8rl_status device_state(DeviceState** out) {
   return FP8RL_OK;
 }
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+fp8rl_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                             uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                             uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle,
+                             const char* what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FP8RL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(FP8RL_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what, (int)r);
+  return FP8RL_OK;
+}
+
 }  // namespace fp8rl
 
 using namespace fp8rl;
@@ -95,7 +131,7 @@ extern "C" fp8rl_status fp8rl_device_status(int32_t device, int32_t clear) {
   }
   if (device != prev) cudaSetDevice(prev);
   if (st != FP8RL_OK) return st;
-  if (words[0] & kStatusGemmTimeout)
-    return fail(FP8RL_ERR_TIMEOUT, "a GEMM pipeline wait hit its time limit (site %u)", words[1]);
+  if (words[0] & kStatusTimeout)
+    return fail(FP8RL_ERR_TIMEOUT, "a kernel pipeline wait hit its time limit (site %u)", words[1]);
   return ok();
 }

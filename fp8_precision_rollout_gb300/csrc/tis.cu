@@ -7,7 +7,8 @@
 // Here d = fl32(logp_train - logp_rollout), e = RN32(e^d) exactly (see
 // fp_exact.cuh), w = min(e, c_hi), then max(w, c_lo) when c_lo > 0, NaN kept,
 // and w = 0 for masked-out tokens.  Elementwise and HBM-bound: 16-byte loads
-// of 4 tokens per thread, grid-stride.
+// of 4 tokens per thread, grid-stride; the exponential's tables live in
+// shared memory.
 #include <cmath>
 
 #include "fp_exact.cuh"
@@ -29,7 +30,19 @@ __global__ void __launch_bounds__(256) tis_kernel(const float* __restrict__ lt,
                                                   const float* __restrict__ lr,
                                                   const uint8_t* __restrict__ mask, int64_t n,
                                                   float c_hi, float c_lo, float* __restrict__ w,
-                                                  const __grid_constant__ fx::Exp2Table T) {
+                                                  const __grid_constant__ fx::Exp2Table Tp) {
+  // lanes index the table with their own j: shared memory serves that in one
+  // pass (32 consecutive words), the parameter bank would serialize it
+  __shared__ fx::Exp2Table T;
+  for (int i = threadIdx.x; i < 32; i += blockDim.x) {
+    T.hi[i] = Tp.hi[i];
+    T.lo[i] = Tp.lo[i];
+  }
+  for (int i = threadIdx.x; i < 12; i += blockDim.x) {
+    T.inv_hi[i] = Tp.inv_hi[i];
+    T.inv_lo[i] = Tp.inv_lo[i];
+  }
+  __syncthreads();
   const int64_t n4 = n >> 2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -60,16 +73,6 @@ __global__ void __launch_bounds__(256) tis_kernel(const float* __restrict__ lt,
   }
 }
 
-fx::Exp2Table make_table() {
-  fx::Exp2Table T;
-  for (int j = 0; j < 32; ++j) {
-    const double v = exp2(j / 32.0);
-    T.hi[j] = (float)v;
-    T.lo[j] = (float)(v - (double)T.hi[j]);
-  }
-  return T;
-}
-
 }  // namespace
 }  // namespace fp8rl
 
@@ -89,7 +92,7 @@ extern "C" fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* 
   fp8rl_status st = device_state(&ds);
   if (st != FP8RL_OK) return st;
   if (n == 0) return ok();
-  static const fx::Exp2Table T = make_table();
+  static const fx::Exp2Table T = fx::make_exp_tables();
   const int64_t threads_needed = std::max<int64_t>((n + 3) / 4, 1);
   int64_t ctas = (threads_needed + 255) / 256;
   ctas = std::min<int64_t>(ctas, (int64_t)ds->sm_count * 8);

@@ -99,7 +99,7 @@ fp8rl_status fp8rl_quantize_weights_blockwise(const void* w, int64_t n, int64_t 
  * a whole model; section 3.4.2 notes it is parallel across blocks and layers).
  *   descs   HOST array of `count` descriptors (read during the call only);
  *           each obeys the requirements above; tensors must not overlap.
- * Tensors are processed in launches of up to 256 descriptors. */
+ * Tensors are processed in launches of up to 160 descriptors. */
 fp8rl_status fp8rl_quantize_weights_blockwise_multi(const fp8rl_wdesc* descs, int32_t count,
                                                     cudaStream_t stream);
 

@@ -142,7 +142,7 @@ def test_weight_quant_multi_batches_and_chunking():
     shapes = [(256, 512), (130, 200), (1, 8), (640, 1024), (128, 136), (3, 4096), (129, 129 + 7)]
     shapes = [(n, k - k % 8) for n, k in shapes]
     ws = [workloads.make_weight(n, k, seed=i) for i, (n, k) in enumerate(shapes)]
-    # more tensors than one launch takes (256 descriptors per launch)
+    # more tensors than one launch takes (160 descriptors per launch)
     ws += [workloads.make_weight(8, 16, seed=1000 + i) for i in range(300)]
     qs, ss = fp8rl.quantize_weights_blockwise_multi([w.to(dev) for w in ws])
     torch.cuda.synchronize()
