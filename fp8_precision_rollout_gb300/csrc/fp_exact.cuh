@@ -22,9 +22,12 @@
 //    arithmetic", ACM TOMS 15(2), 1989) with 32 table entries and a degree-6
 //    Taylor polynomial, accurate to ~2^-44 relative; inputs whose result lies
 //    within 2^-40 of a binary32 rounding boundary, or outside |d| <= 87, are
-//    recomputed in double-double arithmetic (argument reduced by ln 2 and
-//    scaled by 2^-8, degree-11 Taylor series, eight squarings; ~2^-95), whose
-//    rounding is then exact.
+//    recomputed more accurately (~2^-64 relative): reduction by ln2/32 in
+//    double-double, e^r - 1 - r by a degree-7 polynomial in double, and a
+//    double-double table of 2^(j/32).  Over all binary32 d no value e^d lies
+//    closer than 2^-52.6 (relative) to a rounding boundary -- found by
+//    enumerating every input within 2^-40 of one with a 60-digit decimal
+//    exponential -- so that accuracy decides every rounding correctly.
 #pragma once
 
 #include <stdint.h>
@@ -131,13 +134,13 @@ FP8RL_HD float scaled_quotient(float x, const ScaleDiv& d) {
 // ---------------------------------------------- correctly rounded e^d ------
 
 // Tables of the exponential, built on the host by make_exp_tables():
-// 2^(j/32), j = 0..31, as float-float pairs, and 1/i, i = 1..11, as
-// double-double pairs.
+// 2^(j/32), j = 0..31, as float-float pairs (fast path) and as double-double
+// pairs (accurate path).
 struct Exp2Table {
   float hi[32];
   float lo[32];
-  double inv_hi[12];
-  double inv_lo[12];
+  double dhi[32];
+  double dlo[32];
 };
 
 FP8RL_HD void two_sum(float a, float b, float& s, float& e) {
@@ -245,32 +248,39 @@ FP8RL_HD float dd_round_to_float(double H, double L) {
   return f;
 }
 
-// Slow path: any binary32 d.  Kept out of line: it runs for a few lanes in
-// ten thousand, and inlining it at every call site would bloat the fast path.
+// Accurate path: any binary32 d.  Kept out of line: it runs for a few lanes
+// in ten thousand, and inlining it at every call site would bloat the fast
+// path.
 FP8RL_HD_OUTLINE float exp_rn32_slow(float d, const Exp2Table& T) {
   if (d != d) return d;
   if (d > 89.0f) return INFINITY;      // e^89 > 2^128: rounds to +inf
   if (d < -104.0f) return 0.0f;        // e^-104 < 2^-150: rounds to +0
-  const double kLn2Hi = 0x1.62e42fefa39efp-1;     // ln 2 as a double-double
-  const double kLn2Lo = 0x1.abc9e3b39803fp-56;
-  double x = (double)d;
-  double k = rint(dmul(x, 0x1.71547652b82fep0));  // ~1/ln2; sets the reduction range
-  double p1 = dmul(k, kLn2Hi);
-  double p1e = dfma(k, kLn2Hi, -p1);
+  // ln2/32 as a double-double (ln 2 = 0x1.62e42fefa39ef35793c7673007e6p-1)
+  const double kCHi = 0x1.62e42fefa39efp-6;
+  const double kCLo = 0x1.abc9e3b39803fp-61;
+  const double x = (double)d;
+  const double kf = rint(dmul(x, 0x1.71547652b82fep+5));   // ~32/ln2; |k| <= 4800
+  const int k = (int)kf;
+  const int j = k & 31;
+  const int m = (k - j) / 32;
+  // r = x - k ln2/32 as rh + rl, |r| <= ~0.0109
+  const double p1 = dmul(kf, kCHi);
+  const double p1e = dfma(kf, kCHi, -p1);
   dd r = dd_two_sum(x, -p1);
-  r = dd_fast(r.hi, dsub(dsub(r.lo, p1e), dmul(k, kLn2Lo)));
-  r.hi = dmul(r.hi, 0x1p-8);                      // exact scaling: |r| <= ~0.0014
-  r.lo = dmul(r.lo, 0x1p-8);
-  // e^r = 1 + r/1 (1 + r/2 (1 + ... (1 + r/11))), truncation < 2^-130
-  dd p{1.0, 0.0};
-  for (int i = 11; i >= 1; --i) {
-    p = dd_mul(p, r);
-    p = dd_mul(p, dd{T.inv_hi[i], T.inv_lo[i]});
-    p = dd_add_one(p);
-  }
-  for (int i = 0; i < 8; ++i) p = dd_mul(p, p);   // (e^(r/256))^256
-  int ki = (int)k;
-  return dd_round_to_float(ldexp(p.hi, ki), ldexp(p.lo, ki));
+  r = dd_fast(r.hi, dsub(dsub(r.lo, p1e), dmul(kf, kCLo)));
+  // q = e^rh - 1 - rh (degree 7, truncation < 2^-67), in double
+  const double rh = r.hi;
+  double q = dfma(rh, 1.0 / 5040.0, 1.0 / 720.0);
+  q = dfma(rh, q, 1.0 / 120.0);
+  q = dfma(rh, q, 1.0 / 24.0);
+  q = dfma(rh, q, 1.0 / 6.0);
+  q = dfma(rh, q, 0.5);
+  q = dmul(dmul(rh, rh), q);
+  // e^r = 1 + rh + (rl + q + rh*rl) as a double-double
+  dd e = dd_two_sum(1.0, rh);
+  e = dd_fast(e.hi, dadd(e.lo, dadd(r.lo, dfma(rh, r.lo, q))));
+  const dd v = dd_mul(e, dd{T.dhi[j], T.dlo[j]});
+  return dd_round_to_float(ldexp(v.hi, m), ldexp(v.lo, m));
 }
 
 FP8RL_HD float exp_rn32(float d, const Exp2Table& T) {
@@ -279,21 +289,34 @@ FP8RL_HD float exp_rn32(float d, const Exp2Table& T) {
   return exp_rn32_slow(d, T);
 }
 
-// Host-side construction of the tables (C library exp2 in double, good to
-// ~2^-52; the float-float pairs keep 48 bits, the fast path's error budget
-// allows 2^-44).  1/i is split exactly: lo = RN((1 - hi*i) / i) with the
-// residual 1 - hi*i formed exactly by an FMA.
+// Host-side construction of the tables.  2^(j/32) = e^(j ln2/32) is formed
+// in double-double by a Taylor series of e^(x/256) followed by eight
+// squarings (~2^-95); the float-float pairs keep its leading 48 bits.
+inline dd dd_exp_host(dd x) {
+  dd inv[16];
+  for (int i = 1; i < 16; ++i) {
+    inv[i].hi = 1.0 / i;
+    inv[i].lo = fma(-inv[i].hi, (double)i, 1.0) / i;   // exact residual
+  }
+  const dd r{x.hi * 0x1p-8, x.lo * 0x1p-8};
+  dd p{1.0, 0.0};
+  for (int i = 15; i >= 1; --i) p = dd_add_one(dd_mul(dd_mul(p, r), inv[i]));
+  for (int i = 0; i < 8; ++i) p = dd_mul(p, p);
+  return p;
+}
+
 inline Exp2Table make_exp_tables() {
   Exp2Table T;
+  const double kCHi = 0x1.62e42fefa39efp-6, kCLo = 0x1.abc9e3b39803fp-61;  // ln2/32
   for (int j = 0; j < 32; ++j) {
-    const double v = exp2(j / 32.0);
-    T.hi[j] = (float)v;
-    T.lo[j] = (float)(v - (double)T.hi[j]);
-  }
-  T.inv_hi[0] = T.inv_lo[0] = 0.0;
-  for (int i = 1; i < 12; ++i) {
-    T.inv_hi[i] = 1.0 / i;
-    T.inv_lo[i] = fma(-T.inv_hi[i], (double)i, 1.0) / i;
+    const double ph = j * kCHi;
+    const double pe = fma((double)j, kCHi, -ph);
+    const dd x = dd_fast(ph, pe + j * kCLo);
+    const dd v = dd_exp_host(x);
+    T.dhi[j] = v.hi;
+    T.dlo[j] = v.lo;
+    T.hi[j] = (float)v.hi;
+    T.lo[j] = (float)((v.hi - (double)T.hi[j]) + v.lo);
   }
   return T;
 }

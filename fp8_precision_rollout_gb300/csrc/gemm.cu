@@ -19,11 +19,16 @@
 // Kernel shape (one CTA per SM, persistent over output tiles):
 //   tile 128 (M) x 256 (N), k-block 128; 4-stage TMA ring of 48 KB stages
 //   (A 128x128 + B 256x128 bytes, 128-byte swizzle);
-//   warp 0     TMA producer (one elected lane),
-//   warp 1     TMEM allocator and MMA issuer (tcgen05.mma kind::f8f6f4,
-//              M=128 N=256 K=32, four per k-block, one elected lane),
-//   warps 2-9  epilogue: warp w reads TMEM lanes 32*(w%4).. and column half
-//              (w-2)/4, 128 FP32 accumulators per thread.
+//   warp 0      TMA producer (lane 0),
+//   warps 1, 2  MMA issuers (tcgen05.mma kind::f8f6f4, M=128 N=256 K=32, four
+//               per k-block, lane 0): warp 1 issues the even k-blocks into
+//               TMEM partial buffer 0, warp 2 the odd ones into buffer 1.
+//               One thread alone spends longer issuing a k-block (barrier
+//               waits, fence, four MMAs, two commits) than the tensor core
+//               spends executing it; two alternating issuers keep it busy.
+//               Each warp's commits track only its own MMAs.
+//   warps 3-10  epilogue: warp w reads TMEM lanes 32*(w%4).. and column half
+//               (w-3)/4, 128 FP32 accumulators per thread.
 //   TMEM: two 256-column partial buffers (all 512 columns), so the MMA of
 //   k-block kb+1 overlaps the promotion of kb.
 // Every wait on an mbarrier is bounded (1 s); on expiry the kernel records it
@@ -40,7 +45,7 @@ namespace fp8rl {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;            // 11 warps
 constexpr int kAStage = BM * BK;                 // 16 KB
 constexpr int kBStage = BN * BK;                 // 32 KB
 constexpr int kStageBytes = kAStage + kBStage;   // 48 KB
@@ -236,54 +241,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer --
-    uint32_t it = 0;
-    bool alive = true;
-    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
-      const Tile tl = decode_tile<kGrouped>(t, g, st);
-      for (int kb = 0; kb < KB; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1u;
-        bool okw = true;
-        if (lane == 0) okw = mbar_wait(smem_u32(&st->empty[s]), ph ^ 1u, abort_flag, g.status, 1);
-        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-        if (!okw) { alive = false; break; }
-        if (lane == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool alive = true;
+      for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+        const Tile tl = decode_tile<kGrouped>(t, g, st);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(smem_u32(&st->empty[s]), ph ^ 1u, abort_flag, g.status, 1)) {
+            alive = false;
+            break;
+          }
           const uint32_t fb = smem_u32(&st->full[s]);
           mbar_expect_tx(fb, kStageBytes);
           tma_load_2d(smem_u32(sA + s * kAStage), &tmA, fb, kb * BK, tl.m0);
           tma_load_2d(smem_u32(sB + s * kBStage), &tmB, fb, kb * BK, tl.brow);
         }
-        __syncwarp();
       }
-    }
-    if (!alive && lane == 0) {
-      // let the copies already issued land before the CTA can exit
-      const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
-      for (uint32_t j = 1; j <= n; ++j) {
-        const uint32_t i2 = it - j;
-        mbar_drain(smem_u32(&st->full[i2 % STAGES]), (i2 / STAGES) & 1u, g.status, 9);
+      if (!alive) {
+        // let the copies already issued land before the CTA can exit
+        const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+        for (uint32_t j = 1; j <= n; ++j) {
+          const uint32_t i2 = it - j;
+          mbar_drain(smem_u32(&st->full[i2 % STAGES]), (i2 / STAGES) & 1u, g.status, 9);
+        }
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // -------------------------------------------------------- MMA issuer --
-    uint32_t it = 0, kit = 0;
-    bool alive = true;
-    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
-      for (int kb = 0; kb < KB; ++kb, ++it, ++kit) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1u;
-        const int buf = kit & 1;
-        const uint32_t u = kit >> 1;
-        bool okw = true;
-        if (lane == 0) {
-          okw = mbar_wait(smem_u32(&st->tempty[buf]), (u & 1u) ^ 1u, abort_flag, g.status, 2) &&
-                mbar_wait(smem_u32(&st->full[s]), ph, abort_flag, g.status, 3);
-        }
-        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-        if (!okw) { alive = false; break; }
-        tc_fence_after();
-        if (lane == 0) {
+  } else if (warp <= 2) {
+    // ------------------------------------------------------- MMA issuers --
+    // warp 1 takes the k-blocks with even global index, warp 2 the odd ones
+    const uint32_t parity = (uint32_t)(warp - 1);
+    if (lane == 0) {
+      uint32_t it = 0;        // global k-block index (all tiles of this CTA)
+      uint32_t last = 0;
+      bool any = false, alive = true;
+      for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          if ((it & 1u) != parity) continue;
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          const int buf = (int)parity;
+          const uint32_t u = it >> 1;           // use count of this buffer
+          if (!mbar_wait(smem_u32(&st->tempty[buf]), (u & 1u) ^ 1u, abort_flag, g.status, 2) ||
+              !mbar_wait(smem_u32(&st->full[s]), ph, abort_flag, g.status, 3)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
           const uint32_t d = tmem_base + (uint32_t)(buf * BN);
           const uint32_t a0 = smem_u32(sA + s * kAStage);
           const uint32_t b0 = smem_u32(sB + s * kBStage);
@@ -292,20 +298,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f8(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc, kk > 0 ? 1u : 0u);
           mma_commit(smem_u32(&st->empty[s]));
           mma_commit(smem_u32(&st->tfull[buf]));
+          last = it;
+          any = true;
         }
-        __syncwarp();
       }
-    }
-    if (lane == 0 && it > 0) {
-      // the last stage release must have landed before the CTA exits
-      const uint32_t i2 = it - 1;
-      mbar_drain(smem_u32(&st->empty[i2 % STAGES]), (i2 / STAGES) & 1u, g.status, 8);
+      if (any) {
+        // this warp's last stage release must have landed before the CTA exits
+        mbar_drain(smem_u32(&st->empty[last % STAGES]), (last / STAGES) & 1u, g.status, 8);
+      }
     }
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int h = (warp - 2) >> 2;          // column half of the 256-wide tile
+    const int h = (warp - 3) >> 2;          // column half of the 256-wide tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t kit = 0;
     bool alive = true;

@@ -38,9 +38,9 @@ __global__ void __launch_bounds__(256) tis_kernel(const float* __restrict__ lt,
     T.hi[i] = Tp.hi[i];
     T.lo[i] = Tp.lo[i];
   }
-  for (int i = threadIdx.x; i < 12; i += blockDim.x) {
-    T.inv_hi[i] = Tp.inv_hi[i];
-    T.inv_lo[i] = Tp.inv_lo[i];
+  for (int i = threadIdx.x; i < 32; i += blockDim.x) {
+    T.dhi[i] = Tp.dhi[i];
+    T.dlo[i] = Tp.dlo[i];
   }
   __syncthreads();
   const int64_t n4 = n >> 2;
