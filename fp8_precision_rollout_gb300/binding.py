@@ -251,6 +251,28 @@ def tis_weights(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_lo: fl
     return w
 
 
+def quantize_kv_fp8_calibrate_noalloc(x: torch.Tensor, scales: Optional[torch.Tensor] = None,
+                                      q: Optional[torch.Tensor] = None, stream=None):
+    """KV calibrate + quantize without any device allocation by the library
+    (scratch is a fixed 256-head array inside it); same results as
+    quantize_kv_fp8(x, FP8RL_KV_CALIBRATE)."""
+    _dev(x, torch.bfloat16, "x")
+    if not x.is_contiguous() or x.dim() < 2:
+        raise ValueError("x must be a dense [..., heads, head_dim] tensor")
+    heads, hd = x.shape[-2], x.shape[-1]
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(heads, dtype=torch.float32, device=x.device)
+    fn = load().fp8rl_quantize_kv_fp8_calibrate_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    _check(fn(x.data_ptr(), x.numel() // (heads * hd), heads, hd, scales.data_ptr(), q.data_ptr(),
+              _stream(stream)))
+    return q, scales
+
+
 def device_status(device: int = 0, clear: bool = True) -> int:
     """Raises Fp8rlError(FP8RL_ERR_TIMEOUT) if a kernel hit a device-side wait limit."""
     st = load().fp8rl_device_status(device, 1 if clear else 0)

@@ -529,3 +529,94 @@ extern "C" fp8rl_status fp8rl_quantize_kv_fp8(const void* x, int64_t rows, int32
   st = cuda_check(cudaGetLastError(), "kv_quant_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }
+
+// ------------------------------------------ allocation-free KV calibration --
+//
+// Same computation as fp8rl_quantize_kv_fp8(..., FP8RL_KV_CALIBRATE, ...), for
+// callers that cannot have the library allocate device memory: the per-head
+// max slots live in the file-scope array below instead of the library
+// workspace.  Nothing here calls cudaMalloc, cudaFree or any other allocating
+// routine.  The array persists in every device that loads the library until
+// the process exits, is shared by every call of this entry point on that
+// device, and is cleared on the stream at the start of each call.
+
+constexpr int kNoAllocMaxHeads = 256;                 // 1 KB of device memory
+static __device__ __align__(256) uint32_t g_kv_amax_noalloc[kNoAllocMaxHeads];
+
+namespace {
+struct NoAllocDevice {
+  uint32_t* amax = nullptr;   // device address of g_kv_amax_noalloc
+  int sm_count = 0;
+};
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc[64];
+}  // namespace
+
+extern "C" fp8rl_status fp8rl_quantize_kv_fp8_calibrate_noalloc(const void* x, int64_t rows,
+                                                               int32_t heads, int32_t head_dim,
+                                                               float* scales, uint8_t* q,
+                                                               cudaStream_t stream) {
+  if (!x || !scales || !q) return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (rows < 0 || heads < 1 || head_dim < 1)
+    return fail(FP8RL_ERR_INVALID_ARG, "need rows >= 0, heads >= 1, head_dim >= 1");
+  if (heads > kNoAllocMaxHeads)
+    return fail(FP8RL_ERR_UNSUPPORTED_SHAPE,
+                "the allocation-free variant supports at most %d heads (got %d): its scratch is a "
+                "fixed %d-entry device array",
+                kNoAllocMaxHeads, heads, kNoAllocMaxHeads);
+  if (head_dim % 8) return fail(FP8RL_ERR_ALIGNMENT, "head_dim must be a multiple of 8");
+  if ((int64_t)heads * head_dim > 2048)
+    return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "need heads*head_dim <= 2048");
+  if (!aligned(x, 16) || !aligned(q, 8) || !aligned(scales, 4))
+    return fail(FP8RL_ERR_ALIGNMENT, "x must be 16-byte and q 8-byte aligned");
+  int dev = -1;
+  fp8rl_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != FP8RL_OK) return st;
+  if (dev < 0 || dev >= 64) return fail(FP8RL_ERR_UNSUPPORTED_DEVICE, "device %d", dev);
+  NoAllocDevice nd;
+  {
+    // First call on this device (with it current): resolve the array's device
+    // address and the SM count.  Later calls reuse them.
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice& slot = g_noalloc[dev];
+    if (!slot.amax) {
+      int major = 0, minor = 0, sms = 0;
+      st = cuda_check(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev),
+                      "cudaDeviceGetAttribute");
+      if (st == FP8RL_OK)
+        st = cuda_check(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev),
+                        "cudaDeviceGetAttribute");
+      if (st == FP8RL_OK)
+        st = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                        "cudaDeviceGetAttribute");
+      if (st != FP8RL_OK) return st;
+      if (!(major == 10 && minor == 3))
+        return fail(FP8RL_ERR_UNSUPPORTED_DEVICE,
+                    "fp8rl is built for sm_103a (GB300); device %d is sm_%d%d", dev, major, minor);
+      void* ptr = nullptr;
+      st = cuda_check(cudaGetSymbolAddress(&ptr, g_kv_amax_noalloc),
+                      "cudaGetSymbolAddress(g_kv_amax_noalloc)");
+      if (st != FP8RL_OK) return st;
+      slot.amax = static_cast<uint32_t*>(ptr);
+      slot.sm_count = sms;
+    }
+    nd = slot;
+  }
+  KVMap mp;
+  mp.vpr = heads * head_dim / 8;
+  mp.rpp = 256 / mp.vpr;
+  mp.hd = head_dim;
+  const int64_t ctas = rows > 0 ? (rows + mp.rpp - 1) / mp.rpp : 1;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)nd.sm_count * 8));
+  const uint16_t* xb = reinterpret_cast<const uint16_t*>(x);
+  // the slots keep the previous call's maxima: clear the ones this call uses
+  st = cuda_check(cudaMemsetAsync(nd.amax, 0, sizeof(uint32_t) * heads, stream),
+                  "clearing the allocation-free calibration slots");
+  if (st != FP8RL_OK) return st;
+  kv_amax_kernel<<<grid, 256, 0, stream>>>(xb, rows, mp, nd.amax, heads);
+  st = cuda_check(cudaGetLastError(), "kv_amax_kernel launch");
+  if (st != FP8RL_OK) return st;
+  kv_quant_kernel<true><<<grid, 256, 0, stream>>>(xb, rows, mp, nullptr, nd.amax, scales, q, heads);
+  st = cuda_check(cudaGetLastError(), "kv_quant_kernel launch");
+  return st == FP8RL_OK ? ok() : st;
+}

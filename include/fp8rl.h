@@ -162,6 +162,28 @@ fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, const float* s
 fp8rl_status fp8rl_quantize_kv_fp8(const void* x, int64_t rows, int32_t heads, int32_t head_dim,
                                    int32_t mode, float* scales, uint8_t* q, cudaStream_t stream);
 
+/* Allocation-free variant of fp8rl_quantize_kv_fp8(..., FP8RL_KV_CALIBRATE, ...):
+ * the same arguments (minus mode) and bit-identical results.  The paper has
+ * no counterpart for this call; it is an engineering addition.
+ * Some callers cannot let a library allocate device memory: an inference
+ * engine that reserves nearly all of the GPU's memory for its own pools up
+ * front (so a cudaMalloc by a library would fail or fragment that pool),
+ * or a caller that must not risk the implicit device synchronization that
+ * cudaMalloc/cudaFree may cause.  This call uses no cudaMalloc, cudaFree or
+ * other allocating routine: its only scratch (the per-head running maxima)
+ * is a fixed 256-entry (1 KB) array compiled into the library, which each
+ * device that loads the library keeps until the process exits.
+ *   heads    at most 256 (larger values fail with FP8RL_ERR_UNSUPPORTED_SHAPE
+ *            before anything is launched); other requirements as above.
+ * The first call on a device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * Every call on a device shares the one array and clears the slots it uses
+ * at its start, so calls whose executions overlap on the GPU (for instance
+ * on two streams) race and may produce wrong scales: serialize them. */
+fp8rl_status fp8rl_quantize_kv_fp8_calibrate_noalloc(const void* x, int64_t rows, int32_t heads,
+                                                     int32_t head_dim, float* scales, uint8_t* q,
+                                                     cudaStream_t stream);
+
 /* Token-level truncated importance-sampling weights (section 3.4.3):
  *   w[i] = pi_theta / pi_fp8 = exp(logp_train[i] - logp_rollout[i]), truncated:
  *   d = fl32(logp_train - logp_rollout); e = RN32(e^d), the correctly rounded
