@@ -104,6 +104,36 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# The re-quantization kernel's DRAM traffic per element comes from a committed
+# ncu capture (profiles/wquant_kernel_qwen3_8b_layer0.md, line "bench-traffic:");
+# it is reported only while the kernel's sources hash to the captured value.
+WQ_SOURCES = ["fp8_precision_rollout_gb300/csrc/quant.cu",
+              "fp8_precision_rollout_gb300/csrc/fp_exact.cuh",
+              "fp8_precision_rollout_gb300/csrc/sm100_ptx.cuh",
+              "fp8_precision_rollout_gb300/csrc/internal.h"]
+WQ_PROFILE = "profiles/wquant_kernel_qwen3_8b_layer0.md"
+
+
+def sources_sha256(files=WQ_SOURCES) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()
+
+
+def _profiled_traffic(elements: int):
+    path = os.path.join(ROOT, WQ_PROFILE)
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        if line.startswith("bench-traffic:"):
+            d = json.loads(line[len("bench-traffic:"):])
+            if d.get("sources_sha256") == sources_sha256():
+                return d["dram_bytes_per_element"] * elements
+    return None
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -407,7 +437,7 @@ def run_ours(args):
     # the dominant kernel of the step and its roofline
     a1 = rows["a1_requant"]
     dom = {"bound": "hbm", "achieved": a1["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-           "frac": a1["gbs"] / peaks["hbm_gbs"], "traffic": None,
+           "frac": a1["gbs"] / peaks["hbm_gbs"], "traffic": _profiled_traffic(W.req_elems),
            "kernel": "wquant_kernel (a1 re-quantization)",
            "peak_source": peaks["source"] + " hbm_gbs (copy)"}
     if rank == 0:

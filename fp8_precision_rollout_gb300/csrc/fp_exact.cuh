@@ -157,25 +157,35 @@ FP8RL_HD void two_prod(float a, float b, float& p, float& e) {
   e = ffma(a, b, -p);
 }
 
-// Fast path.  Returns false when the input must take exp_rn32_slow (|d| > 87,
-// NaN, or a result too close to a rounding boundary to decide here).
-FP8RL_HD bool exp_rn32_fast(float d, const Exp2Table& T, float* out) {
+// Fast path, in two parts so that a caller can fetch the table entry its own
+// way (the CUDA kernel takes it from lane registers with a warp shuffle):
+// exp_fast_index() gives the table index j of d (any d, also out of range),
+// exp_rn32_fast_with() finishes with th + tl = 2^(j/32).  It returns false
+// when the input must take exp_rn32_slow (|d| > 87, NaN, or a result too close
+// to a rounding boundary to decide here).
+// ln2/32 is split in three: L1 has 12 significant bits so that k*L1 is exact
+// for |k| < 2^12; L2 and L3 carry the next 48 bits.
+constexpr float kExpInvL = 0x1.715476p+5f;      // ~32/ln2; only sets the reduction range
+constexpr float kExpL1 = 0x1.62ep-6f;
+constexpr float kExpL2 = 0x1.0bfbe8p-20f;
+constexpr float kExpL3 = 0x1.cf79acp-45f;
+
+FP8RL_HD int exp_fast_index(float d) {
+  const float kf = rintf(fmul(d, kExpInvL));
+  return fabsf(kf) < 65536.0f ? (((int)kf) & 31) : 0;   // out-of-range d: any valid index
+}
+
+FP8RL_HD bool exp_rn32_fast_with(float d, float th, float tl, float* out) {
   if (!(fabsf(d) <= 87.0f)) return false;
-  // ln2/32 split in three: L1 has 12 significant bits so that k*L1 is exact
-  // for |k| < 2^12; L2 and L3 carry the next 48 bits.
-  const float kInvL = 0x1.715476p+5f;      // ~32/ln2; only sets the reduction range
-  const float L1 = 0x1.62ep-6f;
-  const float L2 = 0x1.0bfbe8p-20f;
-  const float L3 = 0x1.cf79acp-45f;
-  float kf = rintf(fmul(d, kInvL));
+  float kf = rintf(fmul(d, kExpInvL));
   int k = (int)kf;
   // r = d - k*ln2/32 as r_hi + r_lo, |r| <= ~ln2/64
-  float a = ffma(-kf, L1, d);                    // exact
+  float a = ffma(-kf, kExpL1, d);                    // exact
   float p_hi, p_lo;
-  two_prod(kf, L2, p_hi, p_lo);
+  two_prod(kf, kExpL2, p_hi, p_lo);
   float r_hi, e1;
   two_sum(a, -p_hi, r_hi, e1);
-  float r_lo = fsub(fsub(e1, p_lo), fmul(kf, L3));
+  float r_lo = fsub(fsub(e1, p_lo), fmul(kf, kExpL3));
   fast_two_sum(r_hi, r_lo, r_hi, r_lo);
   // e^r - 1 = r + r^2/2 + r^3/6 + r^4/24 + r^5/120 + r^6/720 (+ < 2^-55)
   float sq_hi, sq_lo;
@@ -190,9 +200,8 @@ FP8RL_HD bool exp_rn32_fast(float d, const Exp2Table& T, float* out) {
   fast_two_sum(r_hi, half, s1, e2);
   float p_lo2 = fadd(fadd(fadd(e2, r_lo), half_lo), tail);
   // 2^(j/32) * (1 + P), k = 32 m + j
-  int j = k & 31;
-  int m = (k - j) / 32;
-  float th = T.hi[j], tl = T.lo[j];
+  const int j = k & 31;
+  const int m = (k - j) / 32;
   float m_hi, m_lo;
   two_prod(th, s1, m_hi, m_lo);
   float rest = fadd(fadd(fadd(m_lo, fmul(th, p_lo2)), tl), fmul(tl, fadd(s1, p_lo2)));
@@ -209,6 +218,11 @@ FP8RL_HD bool exp_rn32_fast(float d, const Exp2Table& T, float* out) {
   if (dist <= fmul(yh, 0x1p-40f)) return false;
   *out = fmul(yh, u2f((uint32_t)(m + 127) << 23));   // exact: the result is normal
   return true;
+}
+
+FP8RL_HD bool exp_rn32_fast(float d, const Exp2Table& T, float* out) {
+  const int j = exp_fast_index(d);
+  return exp_rn32_fast_with(d, T.hi[j], T.lo[j], out);
 }
 
 // double-double helpers for the slow path

@@ -31,6 +31,12 @@
 //               (w-3)/4, 128 FP32 accumulators per thread.
 //   TMEM: two 256-column partial buffers (all 512 columns), so the MMA of
 //   k-block kb+1 overlaps the promotion of kb.
+// Decode-sized problems (fewer output tiles than half the SMs) run the
+// split-K flavour: a cluster of 2-4 CTAs per tile, each over a slice of the
+// k-blocks.  Each CTA stages its FP32 partial tile in its own (by then idle)
+// pipeline buffers; rank r then reads rows [r*128/S, (r+1)*128/S) of all S
+// partials through distributed shared memory, sums them in rank order and
+// stores them (reduce-scatter, no global scratch, deterministic).
 // Every wait on an mbarrier is bounded (1 s); on expiry the kernel records it
 // in the library's device status word, drains what it issued and returns.
 #include <cuda_bf16.h>
@@ -44,7 +50,8 @@
 namespace fp8rl {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES_DENSE = 4;
+constexpr int STAGES = STAGES_DENSE;
 constexpr int kThreads = 352;            // 11 warps
 constexpr int kAStage = BM * BK;                 // 16 KB
 constexpr int kBStage = BN * BK;                 // 32 KB
@@ -74,6 +81,16 @@ struct SharedTail {
 
 constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * kStageBytes + sizeof(SharedTail);
 
+// Split-K flavour: a cluster owns exactly one tile, so once its last MMA has
+// completed the stage buffers are idle and hold the FP32 partial tile,
+// [128 rows][kRedLd] (row pitch 1040 B: 16-byte stores by consecutive rows
+// and 16-byte loads along a row are both bank-conflict free).
+constexpr int kRedLd = BN + 4;
+constexpr int kMaxSplit = 4;
+constexpr int kRedBatch = 4;             // row chunks whose loads are in flight together
+static_assert((size_t)BM * kRedLd * sizeof(float) <= (size_t)STAGES * kStageBytes,
+              "the partial tile must fit in the stage buffers");
+
 struct GemmArgs {
   const float* sa;         // [KB, M] group-major activation scales
   const float* sw;         // [E][NB][KB] weight block scales (E = 1 when dense)
@@ -84,6 +101,7 @@ struct GemmArgs {
   const int32_t* offsets;  // grouped: [E+1] device
   int E;                   // grouped: experts
   uint32_t* status;        // library status word
+  int split;               // split-K cluster size (1 = no split)
 };
 
 using namespace ptx;
@@ -199,7 +217,66 @@ __device__ void build_expert_schedule(const GemmArgs& g, SharedTail* st) {
 
 // ----------------------------------------------------------------- kernel --
 
-template <bool kGrouped>
+// Split-K: rank r of S owns rows [128*r/S, 128*(r+1)/S) of the tile.  Its
+// threads read those rows of every rank's staged partial (16-byte loads
+// through distributed shared memory, all of a batch issued before any is
+// used), sum them in rank order and store BF16.  Called by all kThreads
+// threads (et = thread index) once every rank's partial is staged.
+__device__ __forceinline__ void reduce_rows(uint32_t red, int crank, int nsplit, int m0,
+                                            int row_end, int n0, const GemmArgs& g, int et) {
+  const int lo = (BM * crank) / nsplit;
+  const int hi = min((BM * (crank + 1)) / nsplit, row_end - m0);
+  const int tasks = (hi - lo) * (BN / 4);
+  uint32_t base[kMaxSplit];
+#pragma unroll
+  for (int pr = 0; pr < kMaxSplit; ++pr) base[pr] = mapa(red, (uint32_t)(pr < nsplit ? pr : 0));
+  for (int t0 = et; t0 < tasks; t0 += kRedBatch * kThreads) {
+    float4 p[kRedBatch][kMaxSplit];
+#pragma unroll
+    for (int b = 0; b < kRedBatch; ++b) {
+      const int t = t0 + b * kThreads;
+      const int r = lo + t / (BN / 4), c4 = t % (BN / 4);
+      const uint32_t off = (uint32_t)((r * kRedLd + c4 * 4) * (int)sizeof(float));
+#pragma unroll
+      for (int pr = 0; pr < kMaxSplit; ++pr)
+        if (t < tasks && pr < nsplit) p[b][pr] = ld_cluster_v4(base[pr] + off);
+    }
+#pragma unroll
+    for (int b = 0; b < kRedBatch; ++b) {
+      const int t = t0 + b * kThreads;
+      if (t >= tasks) break;
+      const int r = lo + t / (BN / 4), c4 = t % (BN / 4);
+      float4 v = p[b][0];
+#pragma unroll
+      for (int pr = 1; pr < kMaxSplit; ++pr) {
+        if (pr < nsplit) {
+          v.x = __fadd_rn(v.x, p[b][pr].x);
+          v.y = __fadd_rn(v.y, p[b][pr].y);
+          v.z = __fadd_rn(v.z, p[b][pr].z);
+          v.w = __fadd_rn(v.w, p[b][pr].w);
+        }
+      }
+      const int col = n0 + c4 * 4;
+      if (col < g.N) {
+        __nv_bfloat162 b0 = __floats2bfloat162_rn(v.x, v.y);
+        __nv_bfloat162 b1 = __floats2bfloat162_rn(v.z, v.w);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&b0);
+        o.y = *reinterpret_cast<uint32_t*>(&b1);
+        *reinterpret_cast<uint2*>(g.y + (int64_t)(m0 + r) * g.ldy + col) = o;
+      }
+    }
+  }
+}
+
+// kSplit: the CTAs of a thread-block cluster (g.split of them, launched with
+// cluster dimension g.split along x) share one output tile; rank r
+// accumulates k-blocks [r*KB/split, (r+1)*KB/split), then the partials are
+// reduce-scattered over the ranks by rows (see reduce_rows).  Used when there
+// are too few tiles to fill the GPU (decode-sized M); two cluster barrier
+// phases order it: (A) every partial is staged, (B) no CTA reads a peer's
+// shared memory any more (waited for only just before leaving).
+template <bool kGrouped, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmArgs g) {
@@ -209,9 +286,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * kAStage;
   SharedTail* st = reinterpret_cast<SharedTail*>(smem + STAGES * kStageBytes);
+  float* red = reinterpret_cast<float*>(smem);   // split-K: aliases the idle stage buffers
   volatile uint32_t* abort_flag = &st->abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // cluster geometry (a plain launch is a "cluster" of one)
+  const int nsplit = kSplit ? g.split : 1;
+  const uint32_t crank = kSplit ? cluster_ctarank() : 0u;
+  const int cid = kSplit ? (int)(blockIdx.x / nsplit) : (int)blockIdx.x;
+  const int ncl = kSplit ? (int)(gridDim.x / nsplit) : (int)gridDim.x;
+  const int kb_lo = kSplit ? (int)(((int64_t)g.KB * crank) / nsplit) : 0;
+  const int kb_hi = kSplit ? (int)(((int64_t)g.KB * (crank + 1)) / nsplit) : g.KB;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -244,9 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool alive = true;
-      for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+      for (int t = cid; t < total_tiles && alive; t += ncl) {
         const Tile tl = decode_tile<kGrouped>(t, g, st);
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait(smem_u32(&st->empty[s]), ph ^ 1u, abort_flag, g.status, 1)) {
@@ -277,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;        // global k-block index (all tiles of this CTA)
       uint32_t last = 0;
       bool any = false, alive = true;
-      for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+      for (int t = cid; t < total_tiles && alive; t += ncl) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
           if ((it & 1u) != parity) continue;
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -315,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t kit = 0;
     bool alive = true;
-    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+    for (int t = cid; t < total_tiles && alive; t += ncl) {
       const Tile tl = decode_tile<kGrouped>(t, g, st);
       const int row = tl.m0 + q * 32 + lane;
       const bool row_ok = row < tl.row_end;
@@ -327,13 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
       // scales of the next k-block are loaded one iteration ahead so their
       // latency hides behind the current promotion
-      float sa_next = row_ok ? __ldg(g.sa + row) : 0.0f;
-      float sw_next = nb_ok ? __ldg(swp) : 0.0f;
-      for (int kb = 0; kb < KB; ++kb, ++kit) {
+      float sa_next = row_ok ? __ldg(g.sa + (int64_t)kb_lo * g.M + row) : 0.0f;
+      float sw_next = nb_ok ? __ldg(swp + kb_lo) : 0.0f;
+      for (int kb = kb_lo; kb < kb_hi; ++kb, ++kit) {
         const int buf = kit & 1;
         const uint32_t u = kit >> 1;
         const float f = __fmul_rn(sa_next, sw_next);
-        if (kb + 1 < KB) {
+        if (kb + 1 < kb_hi) {
           sa_next = row_ok ? __ldg(g.sa + (int64_t)(kb + 1) * g.M + row) : 0.0f;
           sw_next = nb_ok ? __ldg(swp + kb + 1) : 0.0f;
         }
@@ -358,6 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!alive) break;
+      if (kSplit) {
+        // The last tfull wait above means every MMA of this CTA has completed:
+        // the stage buffers are idle.  Stage this row of the partial there.
+        float* mine = red + (size_t)(q * 32 + lane) * kRedLd + h * 128;
+#pragma unroll
+        for (int j = 0; j < 128; j += 4)
+          *reinterpret_cast<float4*>(mine + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+        continue;
+      }
       if (row_ok) {
         __nv_bfloat16* yrow = g.y + (int64_t)row * g.ldy;
 #pragma unroll
@@ -380,12 +474,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (kSplit) {
+    // Every thread passes both phases exactly once, whatever path it took
+    // (all waits before them are bounded, so every thread gets here).
+    cluster_arrive();   // (A) this thread's part of the partial is staged
+    cluster_wait();
+    const Tile tl = decode_tile<kGrouped>(cid, g, st);
+    reduce_rows(smem_u32(red), (int)crank, nsplit, tl.m0, tl.row_end, tl.n0, g, tid);
+    cluster_arrive();   // (B) this thread reads no peer's shared memory any more
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  if (kSplit) cluster_wait();   // (B): no peer still reads this CTA's shared memory
 }
 
 // ------------------------------------------------------------------- host --
@@ -398,21 +502,61 @@ fp8rl_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
                          CU_TENSOR_MAP_SWIZZLE_128B, what);
 }
 
-template <bool kGrouped>
+template <bool kGrouped, bool kSplit>
 fp8rl_status set_smem_attr(const DeviceState* ds) {
   static bool done[64] = {false};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (ds->device < 64 && done[ds->device]) return FP8RL_OK;
-  if ((size_t)ds->max_smem_optin < kSmemBytes)
+  const size_t bytes = kSmemBytes;
+  if ((size_t)ds->max_smem_optin < bytes)
     return fail(FP8RL_ERR_UNSUPPORTED_DEVICE, "GEMM needs %zu bytes of shared memory per block",
-                kSmemBytes);
+                bytes);
   fp8rl_status st = cuda_check(
-      cudaFuncSetAttribute(gemm_w8a8_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSmemBytes),
+      cudaFuncSetAttribute(gemm_w8a8_kernel<kGrouped, kSplit>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes),
       "cudaFuncSetAttribute(gemm)");
   if (st == FP8RL_OK && ds->device < 64) done[ds->device] = true;
   return st;
+}
+
+// Clusters of `s` split-K CTAs that can be resident at once (0 if unknown).
+int max_active_clusters(const DeviceState* ds, int s) {
+  static int cache[64][kMaxSplit + 1] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  int* c = ds->device < 64 ? &cache[ds->device][s] : nullptr;
+  if (c && *c) return *c;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)s, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)s;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_w8a8_kernel<false, true>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  if (c) *c = n > 0 ? n : -1;
+  return n;
+}
+
+// Split-K cluster size for a dense launch: only when the output tiles cannot
+// fill half the GPU, the largest S <= 4 (and <= the k-blocks) for which one
+// cluster per tile fits in one wave.
+int choose_split(const DeviceState* ds, int64_t tiles, int kb) {
+  const int sms = ds->sm_count;
+  if (tiles <= 0 || tiles * 2 > sms) return 1;
+  int s = (int)std::min<int64_t>(kMaxSplit, sms / tiles);
+  for (s = std::min(s, kb); s >= 2; --s)
+    if (max_active_clusters(ds, s) >= tiles) return s;
+  return 1;
 }
 
 fp8rl_status check_common(const uint8_t* qa, const float* sa, const uint8_t* qw, const float* sw,
@@ -448,7 +592,6 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   if (m == 0) return ok();
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FP8RL_OK) return st;
-  if ((st = set_smem_attr<false>(ds)) != FP8RL_OK) return st;
   CUtensorMap tmA, tmB;
   if ((st = make_map(&tmA, qa, (uint64_t)k, (uint64_t)m, BM, "A")) != FP8RL_OK) return st;
   if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)n, BN, "W")) != FP8RL_OK) return st;
@@ -468,9 +611,33 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   g.status = ds->status;
   const int64_t tiles = (int64_t)g.num_m * g.num_n;
   if (tiles > INT32_MAX) return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "too many tiles");
-  const int grid = (int)std::min<int64_t>(tiles, ds->sm_count);
-  gemm_w8a8_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
-  st = cuda_check(cudaGetLastError(), "gemm_w8a8_kernel launch");
+  if ((st = set_smem_attr<false, true>(ds)) != FP8RL_OK) return st;
+  g.split = choose_split(ds, tiles, g.KB);
+  if (g.split == 1) {
+    if ((st = set_smem_attr<false, false>(ds)) != FP8RL_OK) return st;
+    const int grid = (int)std::min<int64_t>(tiles, ds->sm_count);
+    gemm_w8a8_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+    st = cuda_check(cudaGetLastError(), "gemm_w8a8_kernel launch");
+    return st == FP8RL_OK ? ok() : st;
+  }
+  // few tiles: exactly one cluster of g.split CTAs per tile (the kernel's
+  // reduction reuses the stage buffers, so a cluster never takes a second
+  // tile), split along K
+  const int clusters = (int)tiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(clusters * g.split), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)g.split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  st = cuda_check(cudaLaunchKernelEx(&cfg, gemm_w8a8_kernel<false, true>, tmA, tmB, g),
+                  "split-K gemm_w8a8_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }
 
@@ -492,7 +659,7 @@ extern "C" fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, con
   if (m_total == 0) return ok();
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FP8RL_OK) return st;
-  if ((st = set_smem_attr<true>(ds)) != FP8RL_OK) return st;
+  if ((st = set_smem_attr<true, false>(ds)) != FP8RL_OK) return st;
   CUtensorMap tmA, tmB;
   if ((st = make_map(&tmA, qa, (uint64_t)k, (uint64_t)m_total, BM, "A")) != FP8RL_OK) return st;
   if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)num_experts * n, BN, "W")) != FP8RL_OK)
@@ -513,7 +680,8 @@ extern "C" fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, con
   g.status = ds->status;
   const int64_t bound = ((m_total + BM - 1) / BM + num_experts) * (int64_t)g.num_n;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(bound, ds->sm_count));
-  gemm_w8a8_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+  g.split = 1;
+  gemm_w8a8_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
   st = cuda_check(cudaGetLastError(), "grouped gemm_w8a8_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }

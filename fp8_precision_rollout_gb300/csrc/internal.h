@@ -45,4 +45,15 @@ fp8rl_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const 
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
+// CTAs of `kernel` (launched with `threads` threads, no dynamic shared
+// memory) that fit on one SM at once; streaming kernels size their grid to
+// exactly one resident wave (SMs x this) and loop over the remaining work.
+template <class K>
+int resident_ctas_per_sm(K kernel, int threads) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1)
+    n = 1;
+  return n;
+}
+
 }  // namespace fp8rl

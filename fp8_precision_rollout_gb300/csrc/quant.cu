@@ -484,7 +484,8 @@ extern "C" fp8rl_status fp8rl_quantize_act_groupwise(const void* a, int64_t m, i
   const int octets = (kb + 7) / 8;
   const int64_t tasks = m * octets;
   const int64_t ctas = (tasks + 7) / 8;
-  aquant_kernel<<<grid_for(ctas, ds, 8), 256, 0, stream>>>(
+  static const int per_sm = resident_ctas_per_sm(aquant_kernel, 256);
+  aquant_kernel<<<grid_for(ctas, ds, per_sm), 256, 0, stream>>>(
       reinterpret_cast<const uint16_t*>(a), m, k, lda, q, scales, tasks, octets, kb);
   st = cuda_check(cudaGetLastError(), "aquant_kernel launch");
   return st == FP8RL_OK ? ok() : st;

@@ -90,6 +90,40 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ------------------------------------------------- clusters / DSMEM ------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Split cluster barrier, one arrive and one wait per thread and phase; the
+// phase completes once every thread of every CTA of the cluster has arrived.
+// Arrive releases, wait acquires the threads' earlier memory operations at
+// cluster scope (shared memory of other CTAs included).  Not .aligned: the
+// threads of a warp may reach them on different paths.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// 16-byte load from the shared memory of a CTA of the cluster (address from
+// mapa).  Volatile: stays after the cluster barrier wait that precedes it.
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t caddr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(caddr));
+  return v;
+}
+
 // Named barrier over a subset of the CTA's warps (id 1..15).
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

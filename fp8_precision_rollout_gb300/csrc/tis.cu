@@ -7,8 +7,8 @@
 // Here d = fl32(logp_train - logp_rollout), e = RN32(e^d) exactly (see
 // fp_exact.cuh), w = min(e, c_hi), then max(w, c_lo) when c_lo > 0, NaN kept,
 // and w = 0 for masked-out tokens.  Elementwise and HBM-bound: 16-byte loads
-// of 4 tokens per thread, grid-stride; the exponential's tables live in
-// shared memory.
+// of 4 tokens per thread, grid-stride; each lane holds one entry of the
+// 2^(j/32) table in registers and lanes fetch theirs with a warp shuffle.
 #include <cmath>
 
 #include "fp_exact.cuh"
@@ -17,10 +17,17 @@
 namespace fp8rl {
 namespace {
 
-__device__ __forceinline__ float tis_one(float lt, float lr, float c_hi, float c_lo,
-                                         const fx::Exp2Table& T) {
+// One token.  th_lane / tl_lane hold 2^(lane/32) (float-float) in this lane;
+// every lane of the warp calls this together (the table lookup is a warp
+// shuffle), before any per-lane branch.
+__device__ __forceinline__ float tis_one(float lt, float lr, float c_hi, float c_lo, float th_lane,
+                                         float tl_lane, const fx::Exp2Table& T) {
   const float d = fx::fsub(lt, lr);
-  const float e = fx::exp_rn32(d, T);
+  const int j = fx::exp_fast_index(d);
+  const float th = __shfl_sync(0xFFFFFFFFu, th_lane, j);
+  const float tl = __shfl_sync(0xFFFFFFFFu, tl_lane, j);
+  float e;
+  if (!fx::exp_rn32_fast_with(d, th, tl, &e)) e = fx::exp_rn32_slow(d, T);
   float w = (e > c_hi) ? c_hi : e;
   if (c_lo > 0.0f && e < c_lo) w = c_lo;
   return w;
@@ -30,46 +37,48 @@ __global__ void __launch_bounds__(256) tis_kernel(const float* __restrict__ lt,
                                                   const float* __restrict__ lr,
                                                   const uint8_t* __restrict__ mask, int64_t n,
                                                   float c_hi, float c_lo, float* __restrict__ w,
-                                                  const __grid_constant__ fx::Exp2Table Tp) {
-  // lanes index the table with their own j: shared memory serves that in one
-  // pass (32 consecutive words), the parameter bank would serialize it
-  __shared__ fx::Exp2Table T;
-  for (int i = threadIdx.x; i < 32; i += blockDim.x) {
-    T.hi[i] = Tp.hi[i];
-    T.lo[i] = Tp.lo[i];
-  }
-  for (int i = threadIdx.x; i < 32; i += blockDim.x) {
-    T.dhi[i] = Tp.dhi[i];
-    T.dlo[i] = Tp.dlo[i];
-  }
-  __syncthreads();
+                                                  const __grid_constant__ fx::Exp2Table T) {
+  const int lane = threadIdx.x & 31;
+  const float th_lane = T.hi[lane];
+  const float tl_lane = T.lo[lane];
   const int64_t n4 = n >> 2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(lt) + i);
-    const float4 b = __ldg(reinterpret_cast<const float4*>(lr) + i);
-    float4 r;
-    r.x = tis_one(a.x, b.x, c_hi, c_lo, T);
-    r.y = tis_one(a.y, b.y, c_hi, c_lo, T);
-    r.z = tis_one(a.z, b.z, c_hi, c_lo, T);
-    r.w = tis_one(a.w, b.w, c_hi, c_lo, T);
-    if (mask) {
-      const uint32_t mk = __ldg(reinterpret_cast<const unsigned int*>(mask) + i);
-      if (!(mk & 0xFFu)) r.x = 0.0f;
-      if (!(mk & 0xFF00u)) r.y = 0.0f;
-      if (!(mk & 0xFF0000u)) r.z = 0.0f;
-      if (!(mk & 0xFF000000u)) r.w = 0.0f;
+  // uniform trip count per warp so that every lane reaches the shuffles
+  const int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
+  for (int64_t i0 = base; i0 < n4; i0 += stride) {
+    const int64_t i = i0 + lane;
+    const bool in = i < n4;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (in) {
+      a = __ldg(reinterpret_cast<const float4*>(lt) + i);
+      b = __ldg(reinterpret_cast<const float4*>(lr) + i);
     }
-    reinterpret_cast<float4*>(w)[i] = r;
+    float4 r;
+    r.x = tis_one(a.x, b.x, c_hi, c_lo, th_lane, tl_lane, T);
+    r.y = tis_one(a.y, b.y, c_hi, c_lo, th_lane, tl_lane, T);
+    r.z = tis_one(a.z, b.z, c_hi, c_lo, th_lane, tl_lane, T);
+    r.w = tis_one(a.w, b.w, c_hi, c_lo, th_lane, tl_lane, T);
+    if (in) {
+      if (mask) {
+        const uint32_t mk = __ldg(reinterpret_cast<const unsigned int*>(mask) + i);
+        if (!(mk & 0xFFu)) r.x = 0.0f;
+        if (!(mk & 0xFF00u)) r.y = 0.0f;
+        if (!(mk & 0xFF0000u)) r.z = 0.0f;
+        if (!(mk & 0xFF000000u)) r.w = 0.0f;
+      }
+      reinterpret_cast<float4*>(w)[i] = r;
+    }
   }
-  // ragged tail (n % 4 tokens)
+  // ragged tail (n % 4 tokens): the first warp of block 0
   const int64_t tail = n - (n4 << 2);
-  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gt < tail) {
-    const int64_t j = (n4 << 2) + gt;
-    float r = tis_one(lt[j], lr[j], c_hi, c_lo, T);
-    if (mask && !mask[j]) r = 0.0f;
-    w[j] = r;
+  if (blockIdx.x == 0 && threadIdx.x < 32) {
+    const int64_t j = (n4 << 2) + lane;
+    const bool in = lane < tail;
+    float r = tis_one(in ? lt[j] : 0.f, in ? lr[j] : 0.f, c_hi, c_lo, th_lane, tl_lane, T);
+    if (in) {
+      if (mask && !mask[j]) r = 0.0f;
+      w[j] = r;
+    }
   }
 }
 
@@ -95,7 +104,8 @@ extern "C" fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* 
   static const fx::Exp2Table T = fx::make_exp_tables();
   const int64_t threads_needed = std::max<int64_t>((n + 3) / 4, 1);
   int64_t ctas = (threads_needed + 255) / 256;
-  ctas = std::min<int64_t>(ctas, (int64_t)ds->sm_count * 8);
+  static const int per_sm = resident_ctas_per_sm(tis_kernel, 256);
+  ctas = std::min<int64_t>(ctas, (int64_t)ds->sm_count * per_sm);
   tis_kernel<<<(unsigned)ctas, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi, c_lo, w,
                                                  T);
   st = cuda_check(cudaGetLastError(), "tis_kernel launch");

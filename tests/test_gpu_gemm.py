@@ -54,7 +54,12 @@ def test_tiny_linear():
 @pytest.mark.parametrize("m,n,k,ldy_pad", [(1, 256, 128, 0), (127, 512, 1024, 8), (129, 272, 256, 0),
                                            (300, 512, 384, 40), (64, 256, 512, 0),
                                            (513, 1024, 2048, 0), (200, 16, 128, 0),
-                                           (1000, 1280, 640, 16)])
+                                           (1000, 1280, 640, 16),
+                                           # split-K clusters: S = 3 with uneven row slices
+                                           # and a ragged last m-tile, S = 2, S = 4 with a
+                                           # ragged n-tile and padded rows
+                                           (200, 768, 384, 0), (500, 4096, 1024, 0),
+                                           (100, 720, 4096, 24)])
 def test_shapes(m, n, k, ldy_pad):
     _full_case(m, n, k, seed=m + n + k, ldy_pad=ldy_pad)
 
@@ -141,11 +146,43 @@ def test_grouped_small_with_empty_and_ragged_segments():
     fp8rl.device_status(0)
 
 
+def _agree(y1, y2, absprod):
+    """Two FP32-accumulated, BF16-rounded results of the same product that
+    differ only in summation order: at most one BF16 ulp of the larger, plus
+    FP32 reordering error on the scale of sum |a||w|."""
+    a, b = y1.float().cpu().numpy(), y2.float().cpu().numpy()
+    bound = np.maximum(np.abs(a), np.abs(b)) * 2.0 ** -7 + absprod * 2.0 ** -16
+    assert (np.abs(a - b) <= bound).all()
+
+
 def test_grouped_single_expert_equals_dense():
-    dev = device()
+    """One expert covering every row is the dense GEMM.  The dense call may
+    split K across a cluster (few tiles), which changes only the FP32
+    summation order: both meet the tolerance and differ by at most 1 BF16 ulp."""
+    device()
     qa, sa, qw, sw, off, y, M = _grouped_case([300], 512, 256, seed=22)
     yd = fp8rl.gemm_w8a8_blockwise(qa, sa, qw[0].contiguous(), sw[0].contiguous())
-    assert torch.equal(yd, y)
+    y64, ab = oracle.gemm_w8a8(np_u8(qa), sa.cpu().numpy(), np_u8(qw[0]), sw[0].cpu().numpy())
+    check_gemm(y, y64, ab, "grouped, one expert")
+    check_gemm(yd, y64, ab, "dense")
+    _agree(y, yd, ab)
+
+
+def test_split_k_matches_unsplit_on_many_tiles():
+    """The same product computed with few tiles (split-K cluster path) and as
+    part of a larger launch (one CTA per tile): rows of the small problem must
+    agree with the big one within 1 BF16 ulp, and both meet the tolerance."""
+    dev = device()
+    qa, sa, qw, sw = _quantized(1024, 2048, 1024, seed=23, dev=dev)
+    y_big = fp8rl.gemm_w8a8_blockwise(qa, sa, qw, sw)                 # 8 x 8 tiles: no split
+    qa_s = qa[:128].contiguous()
+    sa_s = sa[:, :128].contiguous()
+    y_small = fp8rl.gemm_w8a8_blockwise(qa_s, sa_s, qw, sw)           # 1 x 8 tiles: split
+    y64, ab = oracle.gemm_w8a8(np_u8(qa_s), sa_s.cpu().numpy(), np_u8(qw), sw.cpu().numpy())
+    check_gemm(y_small, y64, ab, "split-K")
+    check_gemm(y_big[:128], y64, ab, "one CTA per tile")
+    _agree(y_big[:128], y_small, ab)
+    fp8rl.device_status(0)
 
 
 @pytest.mark.parametrize("which", ["gate_up", "down"])
