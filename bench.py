@@ -141,6 +141,22 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(values, device, world):
+    """Element-wise max of per-rank timings (all ranks call it; identity at world 1)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def replica_gbs(world, bytes_per_rank_step, steps, max_ms):
+    """Whole-job throughput of `world` replicas that each move bytes_per_rank_step
+    per step, timed by the slowest rank (GB/s)."""
+    return world * bytes_per_rank_step * steps / (max_ms / 1e3) / 1e9
+
+
 # ----------------------------------------------------------------- workload --
 
 class Workload:
@@ -387,12 +403,9 @@ def run_ours(args):
     fp8rl.device_status(local)
     total_ms = t_start.elapsed_time(t_end)
     a1_ms = sum(_ms(ev, "a1_start", "a1_end"))
-    if world > 1:
-        tt = torch.tensor([total_ms, a1_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms, a1_ms = float(tt[0]), float(tt[1])
+    total_ms, a1_ms = max_over_ranks([total_ms, a1_ms], dev, world)
     rows = _rows(W, ev, args.steps, peaks)
-    value = world * W.req_bytes * args.steps / (a1_ms / 1e3) / 1e9
+    value = replica_gbs(world, W.req_bytes, args.steps, a1_ms)
 
     # e2e: the same re-quantization through the public API from pinned host
     # buffers, host->device copy of the BF16 weights and device->host copy of
@@ -426,11 +439,8 @@ def run_ours(args):
         s1.record()
         barrier()
         e_ms = s0.elapsed_time(s1)
-        if world > 1:
-            tt = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(tt[0])
-        e2e = {"value": world * W.req_bytes * e_steps / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+        e_ms = max_over_ranks([e_ms], dev, world)[0]
+        e2e = {"value": replica_gbs(world, W.req_bytes, e_steps, e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
         del hw, hq, hs
 

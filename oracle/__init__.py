@@ -18,9 +18,10 @@ Each function names the passage of the FP8-RL pages it follows (summary page,
 sections 3.4.1-3.4.4; E4M3 per Micikevicius et al.).
 
 Parity status: every function here is pinned by tests/test_oracle_*.py except
-the two readings the pages leave open -- the KV scale formula (per-head
-amax/448, section 3.4.4 gives no formula) and the MoE routing-bias form of the
-synthetic inputs -- which are marked "parity unpinned" in the design doc.
+two readings the pages leave open, which are parity unpinned: the KV scale
+formula (per-head amax/448; section 3.4.4 gives no formula, so only its
+arithmetic, not the choice of formula, is pinned) and the Zipf form of the
+MoE routing bias in the synthetic inputs (input generation, not method).
 """
 from __future__ import annotations
 

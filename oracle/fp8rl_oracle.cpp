@@ -22,7 +22,7 @@
 //           Learning" (cited by the summary, section 2): bias 7, no infinities,
 //           S.1111.111 is NaN, largest finite magnitude 448.
 //
-// Readings taken where the pages are silent (each restated in the design doc):
+// Readings taken where the pages are silent:
 //   * scale s = fl32(amax / 448) in IEEE binary32 division;
 //   * quantised code = E4M3_RNE_satfinite(fl32(x / s)): two roundings, first
 //     the binary32 quotient, then round-to-nearest-even into E4M3 with
