@@ -283,22 +283,26 @@ fp8rl_status check_wdesc(const fp8rl_wdesc& d, int idx) {
 
 // ------------------------------------------------ 1x128 activation groups --
 
-// A warp task is 8 consecutive groups of one row; 4 lanes per group, each lane
-// 4 x 16-byte chunks (chunk slot + 4i of its group).  Scales go to the
-// group-major array scales[g * m + r].
+// Groups are numbered row-major over the whole matrix, f = r * kb + g (kb =
+// ceil(k/128) groups per row), and a warp task is 8 consecutive groups -- so
+// tasks may span rows and every lane has work even when kb is not a multiple
+// of 8.  4 lanes per group, each lane 4 x 16-byte chunks (chunk slot + 4i of
+// its group).  Scales go to the group-major array scales[g * m + r].
 __global__ void __launch_bounds__(256) aquant_kernel(const uint16_t* __restrict__ a, int64_t m,
                                                      int64_t k, int64_t lda,
                                                      uint8_t* __restrict__ q,
                                                      float* __restrict__ scales,
-                                                     int64_t n_tasks, int octets, int kb) {
+                                                     int64_t n_tasks, int kb) {
   const int lane = threadIdx.x & 31;
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int slot = lane & 3;
+  const int64_t groups = m * kb;
   for (int64_t task = gw; task < n_tasks; task += nw) {
-    const int64_t r = task / octets;
-    const int o = (int)(task - r * octets);
-    const int g = o * 8 + (lane >> 2);
+    const int64_t f = task * 8 + (lane >> 2);
+    const bool valid = f < groups;
+    const int64_t r = valid ? f / kb : 0;
+    const int g = (int)(f - r * kb);
     const int64_t gcol = (int64_t)g * 128;
     const uint16_t* arow = a + r * lda;
     uint4 v[4];
@@ -306,18 +310,18 @@ __global__ void __launch_bounds__(256) aquant_kernel(const uint16_t* __restrict_
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t col = gcol + (slot + 4 * i) * 8;
-      v[i] = (g < kb && col < k) ? ld_stream(arow + col) : make_uint4(0, 0, 0, 0);
+      v[i] = (valid && col < k) ? ld_stream(arow + col) : make_uint4(0, 0, 0, 0);
       m2 = absmax8(m2, v[i]);
     }
     const float amax = warp_max(bf16x2_maxf(m2), 4);
     const float s = fx::fdiv(amax, 448.0f);
-    if (slot == 0 && g < kb) scales[(int64_t)g * m + r] = s;
+    if (slot == 0 && valid) scales[(int64_t)g * m + r] = s;
     const ScaleDiv sd = make_scale_div(s);
     uint8_t* qrow = q + r * k;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t col = gcol + (slot + 4 * i) * 8;
-      if (g < kb && col < k) *reinterpret_cast<uint2*>(qrow + col) = quant8_any<false>(v[i], sd);
+      if (valid && col < k) *reinterpret_cast<uint2*>(qrow + col) = quant8_any<false>(v[i], sd);
     }
   }
 }
@@ -481,12 +485,11 @@ extern "C" fp8rl_status fp8rl_quantize_act_groupwise(const void* a, int64_t m, i
   fp8rl_status st = device_state(&ds);
   if (st != FP8RL_OK) return st;
   const int kb = (int)((k + 127) / 128);
-  const int octets = (kb + 7) / 8;
-  const int64_t tasks = m * octets;
+  const int64_t tasks = (m * kb + 7) / 8;
   const int64_t ctas = (tasks + 7) / 8;
   static const int per_sm = resident_ctas_per_sm(aquant_kernel, 256);
   aquant_kernel<<<grid_for(ctas, ds, per_sm), 256, 0, stream>>>(
-      reinterpret_cast<const uint16_t*>(a), m, k, lda, q, scales, tasks, octets, kb);
+      reinterpret_cast<const uint16_t*>(a), m, k, lda, q, scales, tasks, kb);
   st = cuda_check(cudaGetLastError(), "aquant_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }

@@ -33,7 +33,7 @@ def _act_case(a_cpu, dev, lda_pad=0):
     assert (np_f32_bits(s) == os_.view(np.uint32)).all()
 
 
-@pytest.mark.parametrize("m,k", [(64, 512), (1, 8), (3, 200), (127, 1032), (129, 4104),
+@pytest.mark.parametrize("m,k", [(64, 512), (1, 8), (3, 200), (127, 1032), (129, 4104), (70, 768),
                                  (300, 4096), (256, 12288), (5, 1024 + 24)])
 def test_act_quant_shapes(m, k):
     dev = device()
