@@ -17,8 +17,9 @@
 // the scales of k-block kb+1 are fetched while kb is promoted).
 //
 // Kernel shape (one CTA per SM, persistent over output tiles):
-//   tile 128 (M) x 256 (N), k-block 128; 4-stage TMA ring of 48 KB stages
-//   (A 128x128 + B 256x128 bytes, 128-byte swizzle);
+//   tile 128 (M) x 256 (N), k-block 128; TMA ring of 48 KB stages (A 128x128
+//   + B 256x128 bytes, 128-byte swizzle), 3 stages plus 64 KB of output
+//   staging, or 4 stages in the split-K flavour;
 //   warp 0      TMA producer (lane 0),
 //   warps 1, 2  MMA issuers (tcgen05.mma kind::f8f6f4, M=128 N=256 K=32, four
 //               per k-block, lane 0): warp 1 issues the even k-blocks into
@@ -28,7 +29,9 @@
 //               spends executing it; two alternating issuers keep it busy.
 //               Each warp's commits track only its own MMAs.
 //   warps 3-10  epilogue: warp w reads TMEM lanes 32*(w%4).. and column half
-//               (w-3)/4, 128 FP32 accumulators per thread.
+//               (w-3)/4, 128 FP32 accumulators per thread; a finished tile
+//               is converted to BF16 into the warp's 8 KB staging buffer and
+//               written by TMA tensor stores (plain stores for ragged rows).
 //   TMEM: two 256-column partial buffers (all 512 columns), so the MMA of
 //   k-block kb+1 overlaps the promotion of kb.
 // Decode-sized problems (fewer output tiles than half the SMs) run the
@@ -50,8 +53,12 @@
 namespace fp8rl {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES_DENSE = 4;
-constexpr int STAGES = STAGES_DENSE;
+constexpr int BM = 128, BN = 256, BK = 128;
+// Pipeline depth: the split-K flavour (decode shapes, DRAM-latency bound)
+// keeps 4 stages; the others keep 3 and spend the freed 48 KB on output
+// staging, so the epilogue never waits for its previous tile's stores.
+constexpr int kMaxStages = 4;
+__host__ __device__ constexpr int stages_of(bool split) { return split ? 4 : 3; }
 constexpr int kThreads = 352;            // 11 warps
 constexpr int kAStage = BM * BK;                 // 16 KB
 constexpr int kBStage = BN * BK;                 // 32 KB
@@ -66,8 +73,8 @@ constexpr int kMGroup = 16;                      // m-tiles per raster band (L2 
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
 struct SharedTail {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint32_t tmem_base;
@@ -79,7 +86,17 @@ struct SharedTail {
   int32_t wsum[8];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * kStageBytes + sizeof(SharedTail);
+// Output staging (flavours without split): 8 KB per epilogue warp, its 32 rows
+// x 128 columns as four 32 x 32 BF16 boxes in the 64-byte swizzled layout the
+// Y tensor map describes; after the tail, 1 KB aligned.
+constexpr int kYBox = 32;
+constexpr int kYBoxBytes = kYBox * kYBox * 2;
+constexpr int kYWarpBytes = 4 * kYBoxBytes;
+constexpr size_t kTailPad = (sizeof(SharedTail) + 1023) / 1024 * 1024;
+constexpr size_t smem_bytes(bool split) {
+  return 1024 + (size_t)stages_of(split) * kStageBytes + kTailPad + (split ? 0 : 8 * (size_t)kYWarpBytes);
+}
+static_assert(smem_bytes(false) <= 232448 && smem_bytes(true) <= 232448, "shared memory budget");
 
 // Split-K flavour: a cluster owns exactly one tile, so once its last MMA has
 // completed the stage buffers are idle and hold the FP32 partial tile,
@@ -88,7 +105,7 @@ constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * kStageBytes + sizeof(Share
 constexpr int kRedLd = BN + 4;
 constexpr int kMaxSplit = 4;
 constexpr int kRedBatch = 4;             // row chunks whose loads are in flight together
-static_assert((size_t)BM * kRedLd * sizeof(float) <= (size_t)STAGES * kStageBytes,
+static_assert((size_t)BM * kRedLd * sizeof(float) <= (size_t)stages_of(true) * kStageBytes,
               "the partial tile must fit in the stage buffers");
 
 struct GemmArgs {
@@ -279,7 +296,8 @@ __device__ __forceinline__ void reduce_rows(uint32_t red, int crank, int nsplit,
 template <bool kGrouped, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmArgs g) {
+                     const __grid_constant__ CUtensorMap tmY, const GemmArgs g) {
+  constexpr int STAGES = stages_of(kSplit);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -287,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + STAGES * kAStage;
   SharedTail* st = reinterpret_cast<SharedTail*>(smem + STAGES * kStageBytes);
   float* red = reinterpret_cast<float*>(smem);   // split-K: aliases the idle stage buffers
+  uint8_t* ystage = smem + STAGES * kStageBytes + kTailPad;   // unused by split-K
   volatile uint32_t* abort_flag = &st->abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -312,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
+    if (!kSplit) tma_prefetch_map(&tmY);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&st->tmem_base), kTmemCols);
@@ -452,7 +472,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4*>(mine + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
         continue;
       }
-      if (row_ok) {
+      const int row0 = tl.m0 + q * 32;
+      if (row0 + kYBox <= tl.row_end) {
+        // The warp's 32 rows all belong to this tile: stage them as four
+        // 32 x 32 boxes and write them with TMA tensor stores (the tensor map
+        // clips columns beyond N).  The buffer was last read by the stores of
+        // this warp's previous tile, a whole tile of k-blocks ago.
+        const uint32_t stg = smem_u32(ystage + (warp - 3) * kYWarpBytes);
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float* a8 = acc + c * 32 + j * 8;
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(a8[0], a8[1]);
+            __nv_bfloat162 b1 = __floats2bfloat162_rn(a8[2], a8[3]);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(a8[4], a8[5]);
+            __nv_bfloat162 b3 = __floats2bfloat162_rn(a8[6], a8[7]);
+            // 64-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ ((lane >> 1) & 3)
+            st_shared_v4(stg + (uint32_t)(c * kYBoxBytes + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)),
+                         *reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                         *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col0 = tl.n0 + h * 128 + c * kYBox;
+            if (col0 < g.N) tma_store_2d(&tmY, stg + (uint32_t)(c * kYBoxBytes), col0, row0);
+          }
+          bulk_commit();
+        }
+      } else if (row_ok) {
+        // ragged rows (the last m-tile, or an expert segment's end): plain stores
         __nv_bfloat16* yrow = g.y + (int64_t)row * g.ldy;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -472,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (!kSplit && lane == 0) bulk_wait_all();   // this warp's tensor stores are complete
   }
 
   if (kSplit) {
@@ -496,6 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // 2-D uint8 map over a row-major [rows, inner] matrix, box [box_rows, 128],
 // 128-byte swizzle (the layout the UMMA descriptors describe).
+// BF16 output map over row-major Y [rows, n] (row stride ldy elements), box
+// 32 x 32, 64-byte swizzle (the epilogue's staging layout).
+fp8rl_status make_out_map(CUtensorMap* m, void* y, uint64_t n, uint64_t rows, uint64_t ldy) {
+  return encode_tiled_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, n, rows, ldy * 2, kYBox, kYBox,
+                         CU_TENSOR_MAP_SWIZZLE_64B, "Y");
+}
+
 fp8rl_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
                       uint32_t box_rows, const char* what) {
   return encode_tiled_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner, rows, inner, BK, box_rows,
@@ -508,7 +571,7 @@ fp8rl_status set_smem_attr(const DeviceState* ds) {
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (ds->device < 64 && done[ds->device]) return FP8RL_OK;
-  const size_t bytes = kSmemBytes;
+  const size_t bytes = smem_bytes(kSplit);
   if ((size_t)ds->max_smem_optin < bytes)
     return fail(FP8RL_ERR_UNSUPPORTED_DEVICE, "GEMM needs %zu bytes of shared memory per block",
                 bytes);
@@ -530,7 +593,7 @@ int max_active_clusters(const DeviceState* ds, int s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)s, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes(true);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)s;
@@ -595,6 +658,8 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   CUtensorMap tmA, tmB;
   if ((st = make_map(&tmA, qa, (uint64_t)k, (uint64_t)m, BM, "A")) != FP8RL_OK) return st;
   if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)n, BN, "W")) != FP8RL_OK) return st;
+  CUtensorMap tmY;
+  if ((st = make_out_map(&tmY, y, (uint64_t)n, (uint64_t)m, (uint64_t)ldy)) != FP8RL_OK) return st;
   GemmArgs g;
   g.sa = sa;
   g.sw = sw;
@@ -616,7 +681,7 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   if (g.split == 1) {
     if ((st = set_smem_attr<false, false>(ds)) != FP8RL_OK) return st;
     const int grid = (int)std::min<int64_t>(tiles, ds->sm_count);
-    gemm_w8a8_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+    gemm_w8a8_kernel<false, false><<<grid, kThreads, smem_bytes(false), stream>>>(tmA, tmB, tmY, g);
     st = cuda_check(cudaGetLastError(), "gemm_w8a8_kernel launch");
     return st == FP8RL_OK ? ok() : st;
   }
@@ -627,7 +692,7 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(clusters * g.split), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes(true);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -636,7 +701,7 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  st = cuda_check(cudaLaunchKernelEx(&cfg, gemm_w8a8_kernel<false, true>, tmA, tmB, g),
+  st = cuda_check(cudaLaunchKernelEx(&cfg, gemm_w8a8_kernel<false, true>, tmA, tmB, tmY, g),
                   "split-K gemm_w8a8_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }
@@ -664,6 +729,9 @@ extern "C" fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, con
   if ((st = make_map(&tmA, qa, (uint64_t)k, (uint64_t)m_total, BM, "A")) != FP8RL_OK) return st;
   if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)num_experts * n, BN, "W")) != FP8RL_OK)
     return st;
+  CUtensorMap tmY;
+  if ((st = make_out_map(&tmY, y, (uint64_t)n, (uint64_t)m_total, (uint64_t)n)) != FP8RL_OK)
+    return st;
   GemmArgs g;
   g.sa = sa;
   g.sw = sw;
@@ -681,7 +749,7 @@ extern "C" fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, con
   const int64_t bound = ((m_total + BM - 1) / BM + num_experts) * (int64_t)g.num_n;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(bound, ds->sm_count));
   g.split = 1;
-  gemm_w8a8_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+  gemm_w8a8_kernel<true, false><<<grid, kThreads, smem_bytes(false), stream>>>(tmA, tmB, tmY, g);
   st = cuda_check(cudaGetLastError(), "grouped gemm_w8a8_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }

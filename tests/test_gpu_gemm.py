@@ -54,6 +54,8 @@ def test_tiny_linear():
 @pytest.mark.parametrize("m,n,k,ldy_pad", [(1, 256, 128, 0), (127, 512, 1024, 8), (129, 272, 256, 0),
                                            (300, 512, 384, 40), (64, 256, 512, 0),
                                            (513, 1024, 2048, 0), (200, 16, 128, 0),
+                                           # several tiles per CTA, ragged last n-tile
+                                           (8192, 1392, 256, 8),
                                            (1000, 1280, 640, 16),
                                            # split-K clusters: S = 3 with uneven row slices
                                            # and a ragged last m-tile, S = 2, S = 4 with a
