@@ -87,11 +87,11 @@ struct SharedTail {
 };
 
 // Output staging (flavours without split): 8 KB per epilogue warp, its 32 rows
-// x 128 columns as four 32 x 32 BF16 boxes in the 64-byte swizzled layout the
+// x 128 columns as two 32 x 64 BF16 boxes in the 128-byte swizzled layout the
 // Y tensor map describes; after the tail, 1 KB aligned.
-constexpr int kYBox = 32;
-constexpr int kYBoxBytes = kYBox * kYBox * 2;
-constexpr int kYWarpBytes = 4 * kYBoxBytes;
+constexpr int kYBox = 32, kYBoxCols = 64;
+constexpr int kYBoxBytes = kYBox * kYBoxCols * 2;
+constexpr int kYWarpBytes = 2 * kYBoxBytes;
 constexpr size_t kTailPad = (sizeof(SharedTail) + 1023) / 1024 * 1024;
 constexpr size_t smem_bytes(bool split) {
   return 1024 + (size_t)stages_of(split) * kStageBytes + kTailPad + (split ? 0 : 8 * (size_t)kYWarpBytes);
@@ -474,24 +474,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int row0 = tl.m0 + q * 32;
       if (row0 + kYBox <= tl.row_end) {
-        // The warp's 32 rows all belong to this tile: stage them as four
-        // 32 x 32 boxes and write them with TMA tensor stores (the tensor map
+        // The warp's 32 rows all belong to this tile: stage them as two
+        // 32 x 64 boxes and write them with TMA tensor stores (the tensor map
         // clips columns beyond N).  The buffer was last read by the stores of
         // this warp's previous tile, a whole tile of k-blocks ago.
         const uint32_t stg = smem_u32(ystage + (warp - 3) * kYWarpBytes);
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float* a8 = acc + c * 32 + j * 8;
+          for (int j = 0; j < 8; ++j) {
+            const float* a8 = acc + c * 64 + j * 8;
             __nv_bfloat162 b0 = __floats2bfloat162_rn(a8[0], a8[1]);
             __nv_bfloat162 b1 = __floats2bfloat162_rn(a8[2], a8[3]);
             __nv_bfloat162 b2 = __floats2bfloat162_rn(a8[4], a8[5]);
             __nv_bfloat162 b3 = __floats2bfloat162_rn(a8[6], a8[7]);
-            // 64-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ ((lane >> 1) & 3)
-            st_shared_v4(stg + (uint32_t)(c * kYBoxBytes + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)),
+            // 128-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ (lane & 7)
+            st_shared_v4(stg + (uint32_t)(c * kYBoxBytes + lane * 128 + ((j ^ (lane & 7)) * 16)),
                          *reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
                          *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
           }
@@ -500,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int col0 = tl.n0 + h * 128 + c * kYBox;
+          for (int c = 0; c < 2; ++c) {
+            const int col0 = tl.n0 + h * 128 + c * kYBoxCols;
             if (col0 < g.N) tma_store_2d(&tmY, stg + (uint32_t)(c * kYBoxBytes), col0, row0);
           }
           bulk_commit();
@@ -553,10 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 2-D uint8 map over a row-major [rows, inner] matrix, box [box_rows, 128],
 // 128-byte swizzle (the layout the UMMA descriptors describe).
 // BF16 output map over row-major Y [rows, n] (row stride ldy elements), box
-// 32 x 32, 64-byte swizzle (the epilogue's staging layout).
+// 64 columns x 32 rows, 128-byte swizzle (the epilogue's staging layout).
 fp8rl_status make_out_map(CUtensorMap* m, void* y, uint64_t n, uint64_t rows, uint64_t ldy) {
-  return encode_tiled_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, n, rows, ldy * 2, kYBox, kYBox,
-                         CU_TENSOR_MAP_SWIZZLE_64B, "Y");
+  return encode_tiled_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, n, rows, ldy * 2, kYBoxCols, kYBox,
+                         CU_TENSOR_MAP_SWIZZLE_128B, "Y");
 }
 
 fp8rl_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
