@@ -170,14 +170,18 @@ constexpr float kExpL1 = 0x1.62ep-6f;
 constexpr float kExpL2 = 0x1.0bfbe8p-20f;
 constexpr float kExpL3 = 0x1.cf79acp-45f;
 
-FP8RL_HD int exp_fast_index(float d) {
-  const float kf = rintf(fmul(d, kExpInvL));
+// kf = rint(d * 32/ln2), the reduction multiple of ln2/32 (finite or not).
+FP8RL_HD float exp_fast_k(float d) { return rintf(fmul(d, kExpInvL)); }
+
+FP8RL_HD int exp_fast_index_k(float kf) {
   return fabsf(kf) < 65536.0f ? (((int)kf) & 31) : 0;   // out-of-range d: any valid index
 }
 
-FP8RL_HD bool exp_rn32_fast_with(float d, float th, float tl, float* out) {
+FP8RL_HD int exp_fast_index(float d) { return exp_fast_index_k(exp_fast_k(d)); }
+
+// As exp_rn32_fast_with below, given kf = exp_fast_k(d).
+FP8RL_HD bool exp_rn32_fast_with_k(float d, float kf, float th, float tl, float* out) {
   if (!(fabsf(d) <= 87.0f)) return false;
-  float kf = rintf(fmul(d, kExpInvL));
   int k = (int)kf;
   // r = d - k*ln2/32 as r_hi + r_lo, |r| <= ~ln2/64
   float a = ffma(-kf, kExpL1, d);                    // exact
@@ -218,6 +222,10 @@ FP8RL_HD bool exp_rn32_fast_with(float d, float th, float tl, float* out) {
   if (dist <= fmul(yh, 0x1p-40f)) return false;
   *out = fmul(yh, u2f((uint32_t)(m + 127) << 23));   // exact: the result is normal
   return true;
+}
+
+FP8RL_HD bool exp_rn32_fast_with(float d, float th, float tl, float* out) {
+  return exp_rn32_fast_with_k(d, exp_fast_k(d), th, tl, out);
 }
 
 FP8RL_HD bool exp_rn32_fast(float d, const Exp2Table& T, float* out) {

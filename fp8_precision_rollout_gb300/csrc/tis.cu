@@ -6,9 +6,10 @@
 // experiments; the same section also states the two-sided range [1/C, C]).
 // Here d = fl32(logp_train - logp_rollout), e = RN32(e^d) exactly (see
 // fp_exact.cuh), w = min(e, c_hi), then max(w, c_lo) when c_lo > 0, NaN kept,
-// and w = 0 for masked-out tokens.  Elementwise and HBM-bound: 16-byte loads
-// of 4 tokens per thread, grid-stride; each lane holds one entry of the
-// 2^(j/32) table in registers and lanes fetch theirs with a warp shuffle.
+// and w = 0 for masked-out tokens.  Elementwise: 16-byte loads, 8 tokens per
+// thread per round with all loads issued first, grid-stride; each lane holds
+// one entry of the 2^(j/32) table in registers and lanes fetch theirs with a
+// warp shuffle.
 #include <cmath>
 
 #include "fp_exact.cuh"
@@ -23,16 +24,43 @@ namespace {
 __device__ __forceinline__ float tis_one(float lt, float lr, float c_hi, float c_lo, float th_lane,
                                          float tl_lane, const fx::Exp2Table& T) {
   const float d = fx::fsub(lt, lr);
-  const int j = fx::exp_fast_index(d);
+  const float kf = fx::exp_fast_k(d);
+  const int j = fx::exp_fast_index_k(kf);
   const float th = __shfl_sync(0xFFFFFFFFu, th_lane, j);
   const float tl = __shfl_sync(0xFFFFFFFFu, tl_lane, j);
   float e;
-  if (!fx::exp_rn32_fast_with(d, th, tl, &e)) e = fx::exp_rn32_slow(d, T);
+  if (!fx::exp_rn32_fast_with_k(d, kf, th, tl, &e)) e = fx::exp_rn32_slow(d, T);
   float w = (e > c_hi) ? c_hi : e;
   if (c_lo > 0.0f && e < c_lo) w = c_lo;
   return w;
 }
 
+__device__ __forceinline__ float4 tis_four(float4 a, float4 b, float c_hi, float c_lo,
+                                           float th_lane, float tl_lane, const fx::Exp2Table& T) {
+  float4 r;
+  r.x = tis_one(a.x, b.x, c_hi, c_lo, th_lane, tl_lane, T);
+  r.y = tis_one(a.y, b.y, c_hi, c_lo, th_lane, tl_lane, T);
+  r.z = tis_one(a.z, b.z, c_hi, c_lo, th_lane, tl_lane, T);
+  r.w = tis_one(a.w, b.w, c_hi, c_lo, th_lane, tl_lane, T);
+  return r;
+}
+
+__device__ __forceinline__ void tis_store4(float4 r, int64_t i, const uint8_t* __restrict__ mask,
+                                           float* __restrict__ w) {
+  if (mask) {
+    const uint32_t mk = __ldg(reinterpret_cast<const unsigned int*>(mask) + i);
+    if (!(mk & 0xFFu)) r.x = 0.0f;
+    if (!(mk & 0xFF00u)) r.y = 0.0f;
+    if (!(mk & 0xFF0000u)) r.z = 0.0f;
+    if (!(mk & 0xFF000000u)) r.w = 0.0f;
+  }
+  reinterpret_cast<float4*>(w)[i] = r;
+}
+
+// A warp task is 64 consecutive 4-token vectors: lane l takes vectors l and
+// l + 32, both loaded before either is computed (two DRAM round trips in
+// flight per thread).  Warp-uniform trip count so every lane reaches the
+// shuffles.
 __global__ void __launch_bounds__(256) tis_kernel(const float* __restrict__ lt,
                                                   const float* __restrict__ lr,
                                                   const uint8_t* __restrict__ mask, int64_t n,
@@ -42,32 +70,22 @@ __global__ void __launch_bounds__(256) tis_kernel(const float* __restrict__ lt,
   const float th_lane = T.hi[lane];
   const float tl_lane = T.lo[lane];
   const int64_t n4 = n >> 2;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  // uniform trip count per warp so that every lane reaches the shuffles
-  const int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
-  for (int64_t i0 = base; i0 < n4; i0 += stride) {
-    const int64_t i = i0 + lane;
-    const bool in = i < n4;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-    if (in) {
-      a = __ldg(reinterpret_cast<const float4*>(lt) + i);
-      b = __ldg(reinterpret_cast<const float4*>(lr) + i);
-    }
-    float4 r;
-    r.x = tis_one(a.x, b.x, c_hi, c_lo, th_lane, tl_lane, T);
-    r.y = tis_one(a.y, b.y, c_hi, c_lo, th_lane, tl_lane, T);
-    r.z = tis_one(a.z, b.z, c_hi, c_lo, th_lane, tl_lane, T);
-    r.w = tis_one(a.w, b.w, c_hi, c_lo, th_lane, tl_lane, T);
-    if (in) {
-      if (mask) {
-        const uint32_t mk = __ldg(reinterpret_cast<const unsigned int*>(mask) + i);
-        if (!(mk & 0xFFu)) r.x = 0.0f;
-        if (!(mk & 0xFF00u)) r.y = 0.0f;
-        if (!(mk & 0xFF0000u)) r.z = 0.0f;
-        if (!(mk & 0xFF000000u)) r.w = 0.0f;
-      }
-      reinterpret_cast<float4*>(w)[i] = r;
-    }
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const float4* lt4 = reinterpret_cast<const float4*>(lt);
+  const float4* lr4 = reinterpret_cast<const float4*>(lr);
+  for (int64_t v0 = gw * 64; v0 < n4; v0 += nwarps * 64) {
+    const int64_t i = v0 + lane, i2 = i + 32;
+    const bool in = i < n4, in2 = i2 < n4;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 a = in ? __ldg(lt4 + i) : z;
+    const float4 b = in ? __ldg(lr4 + i) : z;
+    const float4 a2 = in2 ? __ldg(lt4 + i2) : z;
+    const float4 b2 = in2 ? __ldg(lr4 + i2) : z;
+    const float4 r = tis_four(a, b, c_hi, c_lo, th_lane, tl_lane, T);
+    if (in) tis_store4(r, i, mask, w);
+    const float4 r2 = tis_four(a2, b2, c_hi, c_lo, th_lane, tl_lane, T);
+    if (in2) tis_store4(r2, i2, mask, w);
   }
   // ragged tail (n % 4 tokens): the first warp of block 0
   const int64_t tail = n - (n4 << 2);
@@ -102,7 +120,7 @@ extern "C" fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* 
   if (st != FP8RL_OK) return st;
   if (n == 0) return ok();
   static const fx::Exp2Table T = fx::make_exp_tables();
-  const int64_t threads_needed = std::max<int64_t>((n + 3) / 4, 1);
+  const int64_t threads_needed = std::max<int64_t>((n + 7) / 8, 1);   // 8 tokens per thread
   int64_t ctas = (threads_needed + 255) / 256;
   static const int per_sm = resident_ctas_per_sm(tis_kernel, 256);
   ctas = std::min<int64_t>(ctas, (int64_t)ds->sm_count * per_sm);
