@@ -26,6 +26,7 @@ MoE routing bias in the synthetic inputs (input generation, not method).
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 from decimal import Decimal, localcontext
 
@@ -300,6 +301,69 @@ def tis_exp(logp_train, logp_rollout) -> np.ndarray:
 
 
 tis_exp.last_hard_count = 0
+
+
+IS_TRUNCATE, IS_MASK = 0, 1
+
+
+def _sum64(x: np.ndarray) -> float:
+    """Correctly rounded float64 sum of the given values (IEEE propagation of
+    non-finite values)."""
+    x = np.asarray(x, dtype=np.float64).reshape(-1)
+    if not np.isfinite(x).all():
+        return float(np.sum(x))
+    return math.fsum(x.tolist())
+
+
+def is_weights_stats(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_lo: float = 0.0,
+                     mode: int = IS_TRUNCATE):
+    """Importance weights of one batch with their mismatch statistics.
+
+    Summary page, section 3.4.3: the weight w = pi_theta / pi_fp8 =
+    exp(logp_train - logp_rollout); TIS truncates it at C, and the section names
+    masked importance sampling (MIS) as the stronger alternative.  Section
+    "Experimental setup / Metrics" (same page) tracks the mismatch KL
+    D_KL(pi_fp8 || pi_theta) and, for end-to-end FP8, the sampling importance
+    ratio.  Readings (the pages give no estimator):
+
+    * mode IS_TRUNCATE: w as in tis_weights; IS_MASK: w = e if c_lo <= e <= c_hi,
+      else 0 (NaN -> 0).  Masked-out tokens (mask == 0) get w = 0 either way.
+    * over the valid tokens (mask != 0), with d = fl32(lt - lr), e = RN32(e^d):
+      stats[0] = number of valid tokens,
+      stats[1] = sum of fl32(lr - lt)           (k1: its mean estimates the KL,
+                                                 tokens being drawn from pi_fp8),
+      stats[2] = sum of fl32(fl32(e - 1) - d)   (k3 = (r - 1) - log r, r = e^d),
+      stats[3] = sum of e                       (mean = sampling IS ratio),
+      stats[4] = number of valid tokens whose weight was clipped (TIS) or
+                 masked to 0 (MIS).
+      Sums are returned (not means) so that batches can be combined.
+    """
+    lt = np.asarray(logp_train, dtype=np.float32).reshape(-1)
+    lr = np.asarray(logp_rollout, dtype=np.float32).reshape(-1)
+    e = tis_exp(lt, lr).reshape(-1)
+    d = (lt - lr).astype(np.float32)
+    hi, lo = np.float32(c_hi), np.float32(c_lo)
+    if mode == IS_TRUNCATE:
+        w = np.where(e > hi, hi, e)
+        changed = e > hi
+        if c_lo > 0:
+            w = np.where(e < lo, lo, w)
+            changed = changed | (e < lo)
+    elif mode == IS_MASK:
+        keep = (e >= lo) & (e <= hi)
+        w = np.where(keep, e, np.float32(0))
+        changed = ~keep
+    else:
+        raise ValueError("mode must be IS_TRUNCATE or IS_MASK")
+    valid = np.ones(lt.shape, dtype=bool) if mask is None else (np.asarray(mask).reshape(-1) != 0)
+    w = np.where(valid, w, np.float32(0)).astype(np.float32)
+    k1 = (lr - lt).astype(np.float32)
+    k3 = ((e - np.float32(1)).astype(np.float32) - d).astype(np.float32)
+    stats = np.array([float(valid.sum()), _sum64(k1[valid]), _sum64(k3[valid]), _sum64(e[valid]),
+                      float((changed & valid).sum())], dtype=np.float64)
+    terms_abs = np.array([0.0, _sum64(np.abs(k1[valid])), _sum64(np.abs(k3[valid])),
+                          _sum64(np.abs(e[valid])), 0.0])
+    return w, stats, terms_abs
 
 
 def tis_weights(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_lo: float = 0.0):

@@ -95,3 +95,72 @@ def test_clip_mask_nan():
     inf = np.array([np.inf, -np.inf], dtype=np.float32)
     w5 = oracle.tis_weights(inf, np.zeros(2, np.float32))
     assert w5[0] == 2.0 and w5[1] == 0.0
+
+
+# ------------------------------------------------ IS weights + mismatch stats --
+
+def test_is_stats_closed_forms():
+    """lt == lr: every ratio is 1, both KL estimates 0, nothing clipped."""
+    lt = np.linspace(-20, -0.01, 1000).astype(np.float32)
+    for mode in (oracle.IS_TRUNCATE, oracle.IS_MASK):
+        w, st, _ = oracle.is_weights_stats(lt, lt.copy(), mode=mode)
+        assert (w == 1).all()
+        assert list(st) == [1000.0, 0.0, 0.0, 1000.0, 0.0]
+
+
+def test_is_stats_constant_shift_matches_exponential():
+    """d = c for every token: k1 = -c n, sum e = n RN32(e^c), k3 = n fl32(fl32(e - 1) - c);
+    with c = 1 (e > 2) TIS clips every token to 2 and MIS masks every token."""
+    n, c = 777, np.float32(1.0)
+    lr = np.full(n, -3.0, np.float32)
+    lt = (lr + c).astype(np.float32)
+    e1 = np.float32(np.exp(np.float64(1.0)))                # correctly rounded here (checked below)
+    assert e1 == oracle.exp_rn32_decimal(np.float32(1.0))
+    w, st, _ = oracle.is_weights_stats(lt, lr)
+    assert (w == 2).all() and st[4] == n
+    assert st[1] == -float(c) * n
+    assert st[3] == float(e1) * n
+    assert st[2] == float(np.float32(np.float32(e1 - np.float32(1)) - c)) * n
+    w, st, _ = oracle.is_weights_stats(lt, lr, mode=oracle.IS_MASK)
+    assert (w == 0).all() and st[4] == n
+
+
+def test_is_stats_mask_and_ranges():
+    lt, lr = workloads.tis_logprobs(5000, seed=3)
+    lt, lr = lt.numpy(), lr.numpy()
+    e = oracle.tis_exp(lt, lr)
+    mask = (np.arange(5000) % 5 != 0).astype(np.uint8)
+    w, st, _ = oracle.is_weights_stats(lt, lr, mask=mask, mode=oracle.IS_MASK, c_lo=0.5)
+    keep = (e >= 0.5) & (e <= 2) & (mask == 1)
+    assert (w[keep] == e[keep]).all() and (w[~keep] == 0).all()
+    assert st[0] == mask.sum() and st[4] == ((~((e >= 0.5) & (e <= 2))) & (mask == 1)).sum()
+    # excluded tokens do not contribute: same stats as the oracle on the kept subset
+    _, st2, _ = oracle.is_weights_stats(lt[mask == 1], lr[mask == 1], mode=oracle.IS_MASK, c_lo=0.5)
+    assert (st == st2).all()
+    # TIS weights equal tis_weights (same clip), and k1 = -(sum of d) exactly
+    w_t, st_t, _ = oracle.is_weights_stats(lt, lr, mask=mask)
+    assert (w_t == oracle.tis_weights(lt, lr, mask=mask)).all()
+    d = (lt - lr).astype(np.float32)
+    assert st_t[1] == -math.fsum(d[mask == 1].astype(np.float64).tolist())
+
+
+def test_is_stats_estimate_kl_of_gaussian_shift():
+    """Log-ratios d ~ N(0, s^2) with tokens drawn under the rollout policy: the
+    k3 mean estimates E[e^d - 1 - d] = exp(s^2/2) - 1, the ratio mean E[e^d] =
+    exp(s^2/2), the k1 mean E[-d] = 0 (standard errors from the sample)."""
+    rng = np.random.default_rng(31)
+    n, s = 400_000, 0.1
+    lr = -np.abs(rng.normal(0, 2, n)).astype(np.float32)
+    d = rng.normal(0, s, n)
+    lt = (lr.astype(np.float64) + d).astype(np.float32)
+    _, st, _ = oracle.is_weights_stats(lt, lr, c_hi=1e30)
+    dd = (lt - lr).astype(np.float64)
+    want_ratio = math.exp(s * s / 2)
+    assert abs(st[3] / n - want_ratio) < 5 * np.std(np.exp(dd)) / math.sqrt(n)
+    assert abs(st[2] / n - (want_ratio - 1)) < 5 * np.std(np.exp(dd) - 1 - dd) / math.sqrt(n)
+    assert abs(st[1] / n) < 5 * s / math.sqrt(n)
+    # k3 terms are non-negative wherever |d| is large enough to dominate rounding
+    e = oracle.tis_exp(lt, lr)
+    k3 = ((e - np.float32(1)).astype(np.float32) - (lt - lr).astype(np.float32)).astype(np.float32)
+    big = np.abs((lt - lr).astype(np.float32)) >= 2.0 ** -9
+    assert (k3[big] > 0).all()
