@@ -212,6 +212,8 @@ class Workload:
                                 s=torch.empty(8, dtype=torch.float32, device=dev)))
         self.lt, self.lr = wl.tis_logprobs(64 * 20480, seed=5, device=dev, kind="student_t")
         self.tw = torch.empty_like(self.lt)
+        self.mw = torch.empty_like(self.lt)
+        self.is_stats = torch.empty(5, dtype=torch.float64, device=dev)
         torch.cuda.synchronize()
 
     # one step; records an event pair around each row on the current stream
@@ -254,6 +256,10 @@ class Workload:
         fp8rl.tis_weights(self.lt, self.lr, None, 2.0, 0.0, self.tw)
         launches += 1
         mark("tis_end")
+        fp8rl.is_weights_stats(self.lt, self.lr, None, 2.0, 0.5, fp8rl.FP8RL_IS_MASK, w=self.mw,
+                               stats=self.is_stats)
+        launches += 1
+        mark("is_end")
         return launches
 
 
@@ -306,7 +312,11 @@ def _rows(W, ev, steps, peaks):
     t = statistics.mean(_ms(ev, "kv_end", "tis_end"))
     tb = 12 * W.lt.numel()
     out["a6_tis"] = {"ms": t, "bytes": tb, "gbs": tb / t / 1e6, "frac_hbm": tb / t / 1e6 / hbm,
-                     "note": "launch-latency bound at this size"}
+                     "note": "instruction-issue and launch bound at this size"}
+    t = statistics.mean(_ms(ev, "tis_end", "is_end"))
+    out["a6b_mis_stats"] = {"ms": t, "tokens": W.lt.numel(), "bytes": tb,
+                            "gbs": tb / t / 1e6, "frac_hbm": tb / t / 1e6 / hbm,
+                            "note": "MIS weights + mismatch statistics, one pass"}
     return out
 
 

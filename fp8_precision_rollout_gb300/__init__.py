@@ -6,12 +6,15 @@ ctypes layer with the same call names.  The library is loaded on the first
 call and a missing or unloadable library raises -- there is no fallback.
 """
 from .binding import (  # noqa: F401
+    FP8RL_IS_MASK,
+    FP8RL_IS_TRUNCATE,
     FP8RL_KV_CALIBRATE,
     FP8RL_KV_GIVEN,
     Fp8rlError,
     device_status,
     gemm_w8a8_blockwise,
     grouped_gemm_w8a8_blockwise,
+    is_weights_stats,
     last_error,
     quantize_act_groupwise,
     quantize_kv_fp8,

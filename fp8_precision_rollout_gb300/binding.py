@@ -23,6 +23,8 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "fp8rl.h")
 FP8RL_OK = 0
 FP8RL_KV_GIVEN = 0
 FP8RL_KV_CALIBRATE = 1
+FP8RL_IS_TRUNCATE = 0
+FP8RL_IS_MASK = 1
 _STATUS = {0: "FP8RL_OK", 1: "FP8RL_ERR_INVALID_ARG", 2: "FP8RL_ERR_ALIGNMENT",
            3: "FP8RL_ERR_UNSUPPORTED_SHAPE", 4: "FP8RL_ERR_CUDA", 5: "FP8RL_ERR_TIMEOUT",
            6: "FP8RL_ERR_UNSUPPORTED_DEVICE"}
@@ -65,6 +67,7 @@ def load(path: Optional[str] = None):
                                                               P, P]),
         "fp8rl_quantize_kv_fp8": (ctypes.c_int, [P, i64, i32, i32, i32, P, P, P]),
         "fp8rl_tis_weights": (ctypes.c_int, [P, P, P, i64, f32, f32, P, P]),
+        "fp8rl_is_weights_stats": (ctypes.c_int, [P, P, P, i64, f32, f32, i32, P, P, P]),
         "fp8rl_device_status": (ctypes.c_int, [i32, i32]),
     }
     for name, (res, args) in sigs.items():
@@ -249,6 +252,39 @@ def tis_weights(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_lo: fl
     _check(load().fp8rl_tis_weights(logp_train.data_ptr(), logp_rollout.data_ptr(), mp, n,
                                     float(c_hi), float(c_lo), w.data_ptr(), _stream(stream)))
     return w
+
+
+def is_weights_stats(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_lo: float = 0.0,
+                     mode: int = FP8RL_IS_TRUNCATE, w: Optional[torch.Tensor] = None,
+                     stats: Optional[torch.Tensor] = None, weights: bool = True, stream=None):
+    """Importance weights (TIS or MIS by `mode`) and the batch's mismatch
+    statistics [valid tokens, sum k1, sum k3, sum of ratios, clipped/masked
+    tokens] (float64 [5]).  weights=False computes the statistics only.
+    Returns (w or None, stats)."""
+    _dev(logp_train, torch.float32, "logp_train")
+    _dev(logp_rollout, torch.float32, "logp_rollout")
+    n = logp_train.numel()
+    if logp_rollout.numel() != n:
+        raise ValueError("logp_train and logp_rollout must have the same size")
+    wp = 0
+    if weights:
+        if w is None:
+            w = torch.empty_like(logp_train)
+        _dev(w, torch.float32, "w")
+        wp = w.data_ptr()
+    else:
+        w = None
+    if stats is None:
+        stats = torch.empty(5, dtype=torch.float64, device=logp_train.device)
+    _dev(stats, torch.float64, "stats")
+    mp = 0
+    if mask is not None:
+        _dev(mask, torch.uint8, "mask")
+        mp = mask.data_ptr()
+    _check(load().fp8rl_is_weights_stats(logp_train.data_ptr(), logp_rollout.data_ptr(), mp, n,
+                                         float(c_hi), float(c_lo), int(mode), wp,
+                                         stats.data_ptr(), _stream(stream)))
+    return w, stats
 
 
 def quantize_kv_fp8_calibrate_noalloc(x: torch.Tensor, scales: Optional[torch.Tensor] = None,

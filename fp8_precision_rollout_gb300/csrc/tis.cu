@@ -21,15 +21,20 @@ namespace {
 // One token.  th_lane / tl_lane hold 2^(lane/32) (float-float) in this lane;
 // every lane of the warp calls this together (the table lookup is a warp
 // shuffle), before any per-lane branch.
-__device__ __forceinline__ float tis_one(float lt, float lr, float c_hi, float c_lo, float th_lane,
-                                         float tl_lane, const fx::Exp2Table& T) {
-  const float d = fx::fsub(lt, lr);
+// e = RN32(e^d).  Every lane of the warp calls this together (warp shuffles).
+__device__ __forceinline__ float tis_e(float d, float th_lane, float tl_lane, const fx::Exp2Table& T) {
   const float kf = fx::exp_fast_k(d);
   const int j = fx::exp_fast_index_k(kf);
   const float th = __shfl_sync(0xFFFFFFFFu, th_lane, j);
   const float tl = __shfl_sync(0xFFFFFFFFu, tl_lane, j);
   float e;
   if (!fx::exp_rn32_fast_with_k(d, kf, th, tl, &e)) e = fx::exp_rn32_slow(d, T);
+  return e;
+}
+
+__device__ __forceinline__ float tis_one(float lt, float lr, float c_hi, float c_lo, float th_lane,
+                                         float tl_lane, const fx::Exp2Table& T) {
+  const float e = tis_e(fx::fsub(lt, lr), th_lane, tl_lane, T);
   float w = (e > c_hi) ? c_hi : e;
   if (c_lo > 0.0f && e < c_lo) w = c_lo;
   return w;
@@ -100,6 +105,171 @@ __global__ void __launch_bounds__(256) tis_kernel(const float* __restrict__ lt,
   }
 }
 
+// ------------------------------------------ weights + mismatch statistics --
+
+// Float-float running sum (hi + lo), exact up to ~2^-44 relative: FP64 is
+// slow on this part, so FP32 two-sums carry the extra precision.
+struct FF {
+  float hi = 0.f, lo = 0.f;
+  // Once hi is +-inf or NaN it alone carries the IEEE sum (lo would be NaN).
+  __device__ __forceinline__ void add(float x) {
+    float s, e;
+    fx::two_sum(hi, x, s, e);
+    hi = s;
+    lo = fabsf(s) <= 3.402823466e38f ? fx::fadd(lo, e) : 0.f;
+  }
+  __device__ __forceinline__ void add(FF o) {
+    add(o.hi);
+    lo = fabsf(hi) <= 3.402823466e38f ? fx::fadd(lo, o.lo) : 0.f;
+  }
+  __device__ __forceinline__ double value() const { return (double)hi + (double)lo; }
+};
+
+// Running statistics of one thread: FP32 partial sums over the 8 tokens of a
+// round, folded into float-float sums after each round.
+struct IsAcc {
+  float k1 = 0.f, k3 = 0.f, r = 0.f;
+  FF K1, K3, R;
+  int nv = 0, nc = 0;
+  __device__ __forceinline__ void fold() {
+    K1.add(k1);
+    K3.add(k3);
+    R.add(r);
+    k1 = k3 = r = 0.f;
+  }
+};
+
+__device__ __forceinline__ FF warp_sum(FF v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    FF w;
+    w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
+    w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
+    v.add(w);
+  }
+  return v;
+}
+
+// One token: weight by mode (0 = truncate, 1 = mask), statistics if valid.
+template <int kMode>
+__device__ __forceinline__ float is_one(float lt, float lr, bool valid, float c_hi, float c_lo,
+                                        float th_lane, float tl_lane, const fx::Exp2Table& T,
+                                        IsAcc& acc) {
+  const float d = fx::fsub(lt, lr);
+  const float e = tis_e(d, th_lane, tl_lane, T);
+  float w;
+  bool changed;
+  if (kMode == 0) {
+    w = (e > c_hi) ? c_hi : e;
+    changed = e > c_hi;
+    if (c_lo > 0.0f && e < c_lo) {
+      w = c_lo;
+      changed = true;
+    }
+  } else {
+    const bool keep = (e >= c_lo) && (e <= c_hi);
+    w = keep ? e : 0.0f;
+    changed = !keep;
+  }
+  if (!valid) return 0.0f;
+  acc.k1 = fx::fadd(acc.k1, fx::fsub(lr, lt));
+  acc.k3 = fx::fadd(acc.k3, fx::fsub(fx::fsub(e, 1.0f), d));
+  acc.r = fx::fadd(acc.r, e);
+  acc.nv += 1;
+  acc.nc += changed ? 1 : 0;
+  return w;
+}
+
+template <int kMode>
+__device__ __forceinline__ float4 is_four(float4 a, float4 b, uint32_t valid4, float c_hi,
+                                          float c_lo, float th_lane, float tl_lane,
+                                          const fx::Exp2Table& T, IsAcc& acc) {
+  float4 r;
+  r.x = is_one<kMode>(a.x, b.x, valid4 & 1u, c_hi, c_lo, th_lane, tl_lane, T, acc);
+  r.y = is_one<kMode>(a.y, b.y, valid4 & 2u, c_hi, c_lo, th_lane, tl_lane, T, acc);
+  r.z = is_one<kMode>(a.z, b.z, valid4 & 4u, c_hi, c_lo, th_lane, tl_lane, T, acc);
+  r.w = is_one<kMode>(a.w, b.w, valid4 & 8u, c_hi, c_lo, th_lane, tl_lane, T, acc);
+  return r;
+}
+
+// Valid-token bits of 4-token vector i (bit t: token 4i + t).
+__device__ __forceinline__ uint32_t valid_bits(const uint8_t* __restrict__ mask, int64_t i, bool in) {
+  if (!in) return 0u;
+  if (!mask) return 0xFu;
+  const uint32_t mk = __ldg(reinterpret_cast<const unsigned int*>(mask) + i);
+  return ((mk & 0xFFu) ? 1u : 0u) | ((mk & 0xFF00u) ? 2u : 0u) | ((mk & 0xFF0000u) ? 4u : 0u) |
+         ((mk & 0xFF000000u) ? 8u : 0u);
+}
+
+// Same traversal as tis_kernel; the statistics are reduced per CTA and added
+// to stats[5] (cleared beforehand) with one FP64 atomic each.
+template <int kMode, bool kW>
+__global__ void __launch_bounds__(256) is_stats_kernel(const float* __restrict__ lt,
+                                                       const float* __restrict__ lr,
+                                                       const uint8_t* __restrict__ mask, int64_t n,
+                                                       float c_hi, float c_lo, float* __restrict__ w,
+                                                       double* __restrict__ stats,
+                                                       const __grid_constant__ fx::Exp2Table T) {
+  __shared__ double red[8][5];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float th_lane = T.hi[lane];
+  const float tl_lane = T.lo[lane];
+  const int64_t n4 = n >> 2;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const float4* lt4 = reinterpret_cast<const float4*>(lt);
+  const float4* lr4 = reinterpret_cast<const float4*>(lr);
+  IsAcc acc;
+  for (int64_t v0 = gw * 64; v0 < n4; v0 += nwarps * 64) {
+    const int64_t i = v0 + lane, i2 = i + 32;
+    const bool in = i < n4, in2 = i2 < n4;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 a = in ? __ldg(lt4 + i) : z;
+    const float4 b = in ? __ldg(lr4 + i) : z;
+    const float4 a2 = in2 ? __ldg(lt4 + i2) : z;
+    const float4 b2 = in2 ? __ldg(lr4 + i2) : z;
+    const uint32_t m1 = valid_bits(mask, i, in), m2 = valid_bits(mask, i2, in2);
+    const float4 r = is_four<kMode>(a, b, m1, c_hi, c_lo, th_lane, tl_lane, T, acc);
+    const float4 r2 = is_four<kMode>(a2, b2, m2, c_hi, c_lo, th_lane, tl_lane, T, acc);
+    acc.fold();
+    if (kW) {
+      if (in) reinterpret_cast<float4*>(w)[i] = r;
+      if (in2) reinterpret_cast<float4*>(w)[i2] = r2;
+    }
+  }
+  // ragged tail (n % 4 tokens): the first warp of block 0
+  const int64_t tail = n - (n4 << 2);
+  if (blockIdx.x == 0 && warp == 0 && tail > 0) {
+    const int64_t j = (n4 << 2) + lane;
+    const bool in = lane < tail;
+    const bool valid = in && (!mask || mask[j]);
+    const float r = is_one<kMode>(in ? lt[j] : 0.f, in ? lr[j] : 0.f, valid, c_hi, c_lo, th_lane,
+                                  tl_lane, T, acc);
+    acc.fold();
+    if (kW && in) w[j] = r;
+  }
+  int nv = acc.nv, nc = acc.nc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    nv += __shfl_xor_sync(0xFFFFFFFFu, nv, o);
+    nc += __shfl_xor_sync(0xFFFFFFFFu, nc, o);
+  }
+  const FF k1 = warp_sum(acc.K1), k3 = warp_sum(acc.K3), rr = warp_sum(acc.R);
+  if (lane == 0) {
+    red[warp][0] = (double)nv;
+    red[warp][1] = k1.value();
+    red[warp][2] = k3.value();
+    red[warp][3] = rr.value();
+    red[warp][4] = (double)nc;
+  }
+  __syncthreads();
+  if (threadIdx.x < 5) {
+    double t = 0.0;
+    for (int k = 0; k < (int)(blockDim.x >> 5); ++k) t += red[k][threadIdx.x];
+    atomicAdd(stats + threadIdx.x, t);
+  }
+}
+
 }  // namespace
 }  // namespace fp8rl
 
@@ -127,5 +297,50 @@ extern "C" fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* 
   tis_kernel<<<(unsigned)ctas, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi, c_lo, w,
                                                  T);
   st = cuda_check(cudaGetLastError(), "tis_kernel launch");
+  return st == FP8RL_OK ? ok() : st;
+}
+
+extern "C" fp8rl_status fp8rl_is_weights_stats(const float* logp_train, const float* logp_rollout,
+                                               const uint8_t* mask, int64_t n, float c_hi,
+                                               float c_lo, int32_t mode, float* w, double* stats,
+                                               cudaStream_t stream) {
+  if (!stats || (n > 0 && (!logp_train || !logp_rollout)))
+    return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (n < 0) return fail(FP8RL_ERR_INVALID_ARG, "n must be >= 0");
+  if (mode != FP8RL_IS_TRUNCATE && mode != FP8RL_IS_MASK)
+    return fail(FP8RL_ERR_INVALID_ARG, "mode must be FP8RL_IS_TRUNCATE or FP8RL_IS_MASK");
+  if (!(c_hi > 0.0f) || !std::isfinite(c_hi) || !(c_lo >= 0.0f) || !(c_lo <= c_hi))
+    return fail(FP8RL_ERR_INVALID_ARG, "need 0 <= c_lo <= c_hi, c_hi finite and > 0");
+  if (!aligned(logp_train, 16) || !aligned(logp_rollout, 16) || (w && !aligned(w, 16)) ||
+      (mask && !aligned(mask, 4)) || !aligned(stats, 8))
+    return fail(FP8RL_ERR_ALIGNMENT,
+                "log-prob and weight arrays must be 16-byte aligned, mask 4-byte, stats 8-byte");
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  if (st != FP8RL_OK) return st;
+  st = cuda_check(cudaMemsetAsync(stats, 0, 5 * sizeof(double), stream), "cudaMemsetAsync(stats)");
+  if (st != FP8RL_OK || n == 0) return st == FP8RL_OK ? ok() : st;
+  static const fx::Exp2Table T = fx::make_exp_tables();
+  const int64_t threads_needed = std::max<int64_t>((n + 7) / 8, 1);
+  int64_t ctas = (threads_needed + 255) / 256;
+  static const int per_sm = resident_ctas_per_sm(is_stats_kernel<0, true>, 256);
+  ctas = std::min<int64_t>(ctas, (int64_t)ds->sm_count * per_sm);
+  const unsigned grid = (unsigned)ctas;
+  if (mode == FP8RL_IS_TRUNCATE) {
+    if (w)
+      is_stats_kernel<0, true><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi,
+                                                        c_lo, w, stats, T);
+    else
+      is_stats_kernel<0, false><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi,
+                                                         c_lo, w, stats, T);
+  } else {
+    if (w)
+      is_stats_kernel<1, true><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi,
+                                                        c_lo, w, stats, T);
+    else
+      is_stats_kernel<1, false><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi,
+                                                         c_lo, w, stats, T);
+  }
+  st = cuda_check(cudaGetLastError(), "is_stats_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }

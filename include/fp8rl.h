@@ -198,6 +198,38 @@ fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* logp_rollou
                                const uint8_t* mask, int64_t n, float c_hi, float c_lo, float* w,
                                cudaStream_t stream);
 
+typedef enum fp8rl_is_mode {
+  FP8RL_IS_TRUNCATE = 0,   /* TIS: w = min(e, c_hi), then max(w, c_lo) if c_lo > 0 */
+  FP8RL_IS_MASK = 1        /* MIS: w = e if c_lo <= e <= c_hi, else 0 (NaN e: 0) */
+} fp8rl_is_mode;
+
+/* Importance weights and the batch's mismatch statistics in one pass
+ * (section 3.4.3: the weight pi_theta / pi_fp8, its truncation at C and
+ * masked importance sampling as the stronger correction; the experiments'
+ * metrics: the mismatch KL D_KL(pi_fp8 || pi_theta) and the sampling
+ * importance ratio).  Per token d = fl32(logp_train - logp_rollout) and
+ * e = RN32(e^d) as in fp8rl_tis_weights; w by `mode`; w = 0 where
+ * mask[i] == 0.  Over the valid tokens (mask != 0, all if mask is NULL):
+ *   stats[0]  number of valid tokens
+ *   stats[1]  sum of fl32(logp_rollout - logp_train)  (k1 estimator of the KL:
+ *             tokens are drawn from pi_fp8; divide by stats[0] for the mean)
+ *   stats[2]  sum of fl32(fl32(e - 1) - d)          (k3 estimator, (r-1) - log r)
+ *   stats[3]  sum of e                               (mean: sampling IS ratio)
+ *   stats[4]  valid tokens whose weight was clipped (TIS) or masked (MIS)
+ * The per-token terms are exact binary32 values; the sums are accumulated in
+ * FP32 over 8 tokens at a time, then in float-float and FP64, in an order that can
+ * change from call to call: each sum is within 2^-20 * (sum of |terms|) of
+ * the exact sum of the terms.  Counts are exact.
+ *   logp_train, logp_rollout, mask, c_hi, c_lo  as in fp8rl_tis_weights (the
+ *            arrays may be NULL when n == 0; the statistics are then zeros)
+ *   mode     fp8rl_is_mode
+ *   w        FP32 [n], 16-byte aligned, or NULL (statistics only)
+ *   stats    FP64 [5], 8-byte aligned, overwritten (cleared on `stream`
+ *            first), complete when the call's work on `stream` is. */
+fp8rl_status fp8rl_is_weights_stats(const float* logp_train, const float* logp_rollout,
+                                    const uint8_t* mask, int64_t n, float c_hi, float c_lo,
+                                    int32_t mode, float* w, double* stats, cudaStream_t stream);
+
 /* Synchronizes the device and returns FP8RL_ERR_TIMEOUT if any kernel since
  * the last clear hit a device-side wait limit (FP8RL_OK otherwise); clears
  * the word when clear != 0.  device = CUDA ordinal. */

@@ -76,3 +76,79 @@ def test_every_binary32_log_ratio():
         same = (got.view(np.uint32) == ref.view(np.uint32)) | (np.isnan(got) & np.isnan(ref))
         assert same.all(), "chunk %x: %d mismatches" % (start, (~same).sum())
         del bits, lt, w
+
+
+# ------------------------------------------------ IS weights + mismatch stats --
+
+def _stats_case(lt, lr, dev, mask=None, c_hi=2.0, c_lo=0.0, mode=fp8rl.FP8RL_IS_TRUNCATE,
+                weights=True):
+    n = lt.numel()
+    wc = Canary(max(n, 1), torch.float32, dev)
+    sc = Canary(5, torch.float64, dev)
+    w, st = fp8rl.is_weights_stats(lt.to(dev), lr.to(dev), None if mask is None else mask.to(dev),
+                                   c_hi, c_lo, mode, w=wc.view[:n] if weights else None,
+                                   stats=sc.view, weights=weights)
+    torch.cuda.synchronize()
+    wc.check(); sc.check()
+    ref_w, ref_st, terms_abs = oracle.is_weights_stats(lt.numpy(), lr.numpy(),
+                                                       None if mask is None else mask.numpy(),
+                                                       c_hi, c_lo, mode)
+    if weights:
+        got = w.cpu().numpy()
+        same = (got.view(np.uint32) == ref_w.view(np.uint32)) | (np.isnan(got) & np.isnan(ref_w))
+        assert same.all(), "first mismatch at %s" % np.argwhere(~same)[:5].ravel()
+    else:
+        assert (wc.view.view(torch.int32).cpu() == wc.view.view(torch.int32).cpu()[0]).all()
+    g = st.cpu().numpy()
+    # counts exact; sums within the documented bound 2^-20 * sum |terms|
+    assert g[0] == ref_st[0] and g[4] == ref_st[4]
+    for q in (1, 2, 3):
+        if not np.isfinite(ref_st[q]):   # inf / NaN terms propagate
+            assert g[q] == ref_st[q] or (np.isnan(g[q]) and np.isnan(ref_st[q])), (q, g[q])
+            continue
+        assert abs(g[q] - ref_st[q]) <= 2.0 ** -20 * terms_abs[q] + 1e-300, (q, g[q], ref_st[q])
+    return g, ref_st
+
+
+@pytest.mark.parametrize("mode", [fp8rl.FP8RL_IS_TRUNCATE, fp8rl.FP8RL_IS_MASK])
+def test_is_stats_tiny_and_ragged(mode):
+    dev = device()
+    for n in (4096, 1, 3, 5, 37, 4099, 70001):
+        lt, lr = workloads.tis_logprobs(n, seed=n)
+        _stats_case(lt, lr, dev, mode=mode)
+        _stats_case(lt, lr, dev, mode=mode, c_lo=0.5)
+        mask = (torch.arange(n) % 7 != 3).to(torch.uint8)
+        _stats_case(lt, lr, dev, mask=mask, mode=mode)
+
+
+def test_is_stats_long_context_student_t():
+    dev = device()
+    lt, lr = workloads.tis_logprobs(64 * 20480, seed=5, kind="student_t")
+    for mode in (fp8rl.FP8RL_IS_TRUNCATE, fp8rl.FP8RL_IS_MASK):
+        _stats_case(lt, lr, dev, mode=mode)
+    _stats_case(lt, lr, dev, mode=fp8rl.FP8RL_IS_MASK, c_lo=0.5, weights=False)
+
+
+def test_is_stats_special_values_and_empty():
+    dev = device()
+    lt = torch.tensor([0.0, -1.0, float("nan"), -5.0, 3.0, -100.0, 0.5, -0.5], dtype=torch.float32)
+    lr = torch.tensor([0.0, -2.0, -1.0, float("nan"), -90.0, 0.0, 0.5, -0.25], dtype=torch.float32)
+    # NaN and huge log-ratios: weights bit-exact, statistics propagate NaN / inf like the oracle
+    n = lt.numel()
+    w, st = fp8rl.is_weights_stats(lt.to(dev), lr.to(dev), mode=fp8rl.FP8RL_IS_MASK)
+    ref_w, ref_st, _ = oracle.is_weights_stats(lt.numpy(), lr.numpy(), mode=oracle.IS_MASK)
+    got = w.cpu().numpy()
+    assert ((got.view(np.uint32) == ref_w.view(np.uint32)) | (np.isnan(got) & np.isnan(ref_w))).all()
+    g = st.cpu().numpy()
+    assert g[0] == n and g[4] == ref_st[4]
+    assert np.isnan(g[1]) == np.isnan(ref_st[1]) and np.isnan(g[3]) == np.isnan(ref_st[3])
+    # valid-only statistics without the NaN tokens
+    mask = torch.tensor([1, 1, 0, 0, 1, 1, 1, 1], dtype=torch.uint8)
+    _stats_case(lt, lr, dev, mask=mask, mode=fp8rl.FP8RL_IS_MASK)
+    # empty input: statistics cleared, nothing written
+    e = torch.empty(0, dtype=torch.float32)
+    sc = Canary(5, torch.float64, dev)
+    fp8rl.is_weights_stats(e.to(dev), e.to(dev), stats=sc.view)
+    torch.cuda.synchronize()
+    sc.check()
+    assert (sc.view.cpu().numpy() == 0).all()
