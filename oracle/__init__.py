@@ -69,6 +69,9 @@ def lib():
                                                     P, i64, P, P, ctypes.c_int]
         L.orc_tis_exp.restype = i64
         L.orc_tis_exp.argtypes = [P, P, i64, P, P, i64, ctypes.c_int]
+        L.orc_glue_exp32.argtypes = [P, P, i64, ctypes.c_int]
+        L.orc_float_to_bf16.argtypes = [P, P, i64]
+        L.orc_silu_mul_bf16.argtypes = [P, i64, i64, i64, P, ctypes.c_int]
         _LIB = L
     return _LIB
 
@@ -160,6 +163,51 @@ def quantize_act_groupwise(a):
     s = np.zeros(((k + 127) // 128, m), dtype=np.float32)
     lib().orc_quantize_act_groupwise(_p(ab), m, k, k, _p(q), _p(s), threads())
     return q, s
+
+
+def quantize_act_gather(a, rows):
+    """MoE glue, permute + quantize: the expert-sorted rows a[rows[r]] of the
+    token matrix a, quantized in 1x128 groups (quantize_act_groupwise of the
+    gathered matrix)."""
+    import torch
+    idx = np.asarray(rows, dtype=np.int64)
+    ab = _u16(a)
+    return quantize_act_groupwise(torch.from_numpy(np.ascontiguousarray(ab[idx])).view(torch.bfloat16))
+
+
+def glue_exp32(x) -> np.ndarray:
+    """The MoE glue's binary32 exponential (see glue_exp32 in fp8rl_oracle.cpp)."""
+    xf = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.empty_like(xf)
+    lib().orc_glue_exp32(_p(xf), _p(out), xf.size, threads())
+    return out
+
+
+def float_to_bf16(x) -> np.ndarray:
+    """binary32 -> BF16 bits, round to nearest even."""
+    xf = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.empty(xf.shape, dtype=np.uint16)
+    lib().orc_float_to_bf16(_p(xf), _p(out), xf.size)
+    return out
+
+
+def silu_mul_bf16(h):
+    """MoE glue between the expert GEMMs: h BF16 [m, 2*inter] = [gate | up]
+    (the gate_up projection's output), y = BF16(silu(gate) * up), BF16 [m, inter].
+    silu(g) = g / (1 + e^-g) with the glue exponential; every step one binary32
+    operation, BF16 rounding to nearest even at the end."""
+    import torch
+    hb = _u16(h)
+    m, two_i = hb.shape
+    inter = two_i // 2
+    y = np.empty((m, inter), dtype=np.uint16)
+    lib().orc_silu_mul_bf16(_p(hb), m, inter, two_i, _p(y), threads())
+    return torch.from_numpy(y.view(np.int16)).view(torch.bfloat16)
+
+
+def silu_mul_quantize(h):
+    """silu_mul_bf16 followed by 1x128-group quantization of y."""
+    return quantize_act_groupwise(silu_mul_bf16(h))
 
 
 def kv_calibrate(x):

@@ -126,6 +126,52 @@ float scale_from_amax(float amax) { return amax / 448.0f; }
 
 }  // namespace
 
+
+// ------------------------------------------------------- MoE glue (SiLU) --
+
+// Reading for the MoE SiLU glue (the pages fix no activation arithmetic): the
+// exponential is this algorithm, one IEEE binary32 operation per step, which
+// the GPU restates step for step:
+//   x > 88 -> +inf, x < -86 -> 0 (1 + e^x rounds to 1 there), NaN -> NaN;
+//   k = rint(fl32(x * RN(log2 e)));
+//   r = fma(-k, RN(ln2), x); r = fma(-k, RN(ln2 - RN(ln2)), r)   (Cody-Waite);
+//   p = degree-7 Taylor polynomial of e^r (coefficients RN(1/n!)), Horner
+//       with fma, ending ... fma(p, r, 1), fma(p, r, 1);
+//   e = p * 2^k (an exact product: |k| <= 127, result normal).
+float glue_exp32(float x) {
+  if (x != x) return x;
+  if (x > 88.0f) return INFINITY;
+  if (x < -86.0f) return 0.0f;
+  const float kf = std::rint(x * 0x1.715476p+0f);
+  float r = std::fma(-kf, 0x1.62e43p-1f, x);
+  r = std::fma(-kf, -0x1.05c61p-29f, r);
+  float p = 0x1.a01a02p-13f;            // 1/7!
+  p = std::fma(p, r, 0x1.6c16c2p-10f);  // 1/6!
+  p = std::fma(p, r, 0x1.111112p-7f);   // 1/5!
+  p = std::fma(p, r, 0x1.555556p-5f);   // 1/4!
+  p = std::fma(p, r, 0x1.555556p-3f);   // 1/3!
+  p = std::fma(p, r, 0.5f);
+  p = std::fma(p, r, 1.0f);
+  p = std::fma(p, r, 1.0f);
+  return p * std::ldexp(1.0f, (int)kf);
+}
+
+// silu(g) * u = (g / (1 + e^-g)) * u, each step one binary32 operation.
+float glue_silu_mul(float g, float u) {
+  const float den = 1.0f + glue_exp32(-g);
+  const float s = g / den;
+  return s * u;
+}
+
+// binary32 -> BF16, round to nearest even (NaN stays a quiet NaN).
+uint16_t float_to_bf16(float f) {
+  uint32_t b;
+  std::memcpy(&b, &f, 4);
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((b >> 16) | 0x0040u);
+  b += 0x7FFFu + ((b >> 16) & 1u);
+  return (uint16_t)(b >> 16);
+}
+
 extern "C" {
 
 // ------------------------------------------------------------- the codec --
@@ -401,6 +447,29 @@ int64_t orc_tis_exp(const float* lt, const float* lr, int64_t n, float* e32,
       ++cnt;
     }
   return cnt;
+}
+
+void orc_glue_exp32(const float* x, float* out, int64_t n, int threads) {
+  parallel_for(n, threads, [&](int64_t lo, int64_t hi) {
+    for (int64_t i = lo; i < hi; ++i) out[i] = glue_exp32(x[i]);
+  });
+}
+
+void orc_float_to_bf16(const float* x, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = float_to_bf16(x[i]);
+}
+
+// Gated activation of one MoE expert layer: h is BF16 [m, 2*inter] (row
+// stride ldh) holding gate (columns [0, inter)) then up ([inter, 2*inter));
+// y = BF16(silu(gate) * up), BF16 [m, inter].
+void orc_silu_mul_bf16(const uint16_t* h, int64_t m, int64_t inter, int64_t ldh, uint16_t* y,
+                       int threads) {
+  parallel_for(m, threads, [&](int64_t lo, int64_t hi) {
+    for (int64_t r = lo; r < hi; ++r)
+      for (int64_t c = 0; c < inter; ++c)
+        y[r * inter + c] = float_to_bf16(
+            glue_silu_mul(bf16_to_float(h[r * ldh + c]), bf16_to_float(h[r * ldh + inter + c])));
+  });
 }
 
 }  // extern "C"
