@@ -186,17 +186,20 @@ class Workload:
                 y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
                 self.gemms.append(dict(name=name, m=m, n=n, k=k, a=a, qa=qa, sa=sa, y=y,
                                        qw=self.q[j], sw=self.s[j]))
-        # a4: MoE experts
-        offsets, _, counts = wl.moe_routing(seed=0)
+        # a4 + MoE glue: token matrix -> gather + quantize -> grouped gate_up ->
+        # SiLU(gate) * up + quantize -> grouped down
+        offsets, token_of_row, counts = wl.moe_routing(seed=0)
         self.moe_off = offsets.to(dev)
         self.moe_rows = int(offsets[-1])
+        self.moe_tokens = wl.dense_acts(wl.MOE_TOKENS, wl.MOE_HIDDEN, seed=wl.sub_seed(5, 1),
+                                        device=dev)
+        self.moe_src = token_of_row.to(torch.int32).to(dev)
         self.moe = []
         for which, (n, k) in (("gate_up", (2 * wl.MOE_INTER, wl.MOE_HIDDEN)),
                               ("down", (wl.MOE_HIDDEN, wl.MOE_INTER))):
             w = wl.moe_weights(n, k, wl.MOE_EXPERTS, seed=wl.sub_seed(4, n, k), device=dev)
             qw, sw = fp8rl.quantize_weights_blockwise(w.view(-1, k))
-            a = wl.expert_inputs(self.moe_rows, k, seed=wl.sub_seed(5, n, k), device=dev)
-            self.moe.append(dict(name=which, n=n, k=k, a=a,
+            self.moe.append(dict(name=which, n=n, k=k,
                                  qa=torch.empty(self.moe_rows, k, dtype=torch.uint8, device=dev),
                                  sa=torch.empty(k // 128, self.moe_rows, dtype=torch.float32,
                                                 device=dev),
@@ -242,7 +245,10 @@ class Workload:
         for g in self.moe:
             key = "moe_" + g["name"]
             mark(key + "_start")
-            fp8rl.quantize_act_groupwise(g["a"], g["qa"], g["sa"])
+            if g["name"] == "gate_up":     # glue: gather the routed token rows, quantize
+                fp8rl.quantize_act_gather(self.moe_tokens, self.moe_src, g["qa"], g["sa"])
+            else:                          # glue: SiLU(gate) * up of gate_up's output, quantize
+                fp8rl.silu_mul_quantize(self.moe[0]["y"], g["qa"], g["sa"])
             mark(key + "_mid")
             fp8rl.grouped_gemm_w8a8_blockwise(g["qa"], g["sa"], g["qw"], g["sw"], self.moe_off,
                                               g["y"])
@@ -300,7 +306,13 @@ def _rows(W, ev, steps, peaks):
         gbytes = m * k + 4 * m * k / 128 + 128 * n * k + 128 * 4 * (n / 128) * (k / 128) + 2 * m * n
         ai = flops / gbytes
         attain = min(fp8_sust * 1e12, ai * hbm * 1e9) / 1e12
-        out[key] = {"act_quant_ms": tq, "gemm_ms": tg, "tflops": flops / tg / 1e9,
+        # glue bytes: gather reads k and writes k + scales per row; SiLU glue reads 2k
+        gl_bytes = (2 * m * k if g["name"] == "gate_up" else 4 * m * k) + m * k + 4 * m * k / 128
+        out[key] = {"glue": "gather + quantize" if g["name"] == "gate_up" else
+                    "SiLU(gate)*up + quantize",
+                    "glue_ms": tq, "glue_gbs": gl_bytes / tq / 1e6,
+                    "glue_frac_hbm": gl_bytes / tq / 1e6 / hbm,
+                    "gemm_ms": tg, "tflops": flops / tg / 1e9,
                     "frac_fp8_peak": flops / tg / 1e9 / fp8_sust,
                     "frac_attainable": flops / tg / 1e9 / attain,
                     "bound": "tensor" if ai * hbm * 1e9 > fp8_sust * 1e12 else "hbm"}

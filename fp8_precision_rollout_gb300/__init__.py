@@ -16,10 +16,12 @@ from .binding import (  # noqa: F401
     grouped_gemm_w8a8_blockwise,
     is_weights_stats,
     last_error,
+    quantize_act_gather,
     quantize_act_groupwise,
     quantize_kv_fp8,
     quantize_weights_blockwise,
     quantize_weights_blockwise_multi,
+    silu_mul_quantize,
     tis_weights,
     version,
 )

@@ -68,6 +68,8 @@ def load(path: Optional[str] = None):
         "fp8rl_quantize_kv_fp8": (ctypes.c_int, [P, i64, i32, i32, i32, P, P, P]),
         "fp8rl_tis_weights": (ctypes.c_int, [P, P, P, i64, f32, f32, P, P]),
         "fp8rl_is_weights_stats": (ctypes.c_int, [P, P, P, i64, f32, f32, i32, P, P, P]),
+        "fp8rl_quantize_act_gather": (ctypes.c_int, [P, i64, i64, i64, P, i64, P, P, P]),
+        "fp8rl_silu_mul_quantize": (ctypes.c_int, [P, i64, i64, i64, P, P, P]),
         "fp8rl_device_status": (ctypes.c_int, [i32, i32]),
     }
     for name, (res, args) in sigs.items():
@@ -230,6 +232,48 @@ def grouped_gemm_w8a8_blockwise(qa, sa, qw, sw, offsets, y: Optional[torch.Tenso
                                                     sw.data_ptr(), offsets.data_ptr(), e, m, n,
                                                     k, y.data_ptr(), _stream(stream)))
     return y
+
+
+# --------------------------------------------------------------- MoE glue --
+
+def quantize_act_gather(a, rows, q: Optional[torch.Tensor] = None,
+                        scales: Optional[torch.Tensor] = None, stream=None):
+    """Codes and group-major scales of the gathered rows a[rows[r]] (1x128 groups)."""
+    _dev(a, torch.bfloat16, "a")
+    _rowmajor(a, "a")
+    _dev(rows, torch.int32, "rows")
+    if not rows.is_contiguous():
+        raise ValueError("rows must be contiguous")
+    m_src, k = a.shape
+    m = rows.numel()
+    if q is None:
+        q = torch.empty(m, k, dtype=torch.uint8, device=a.device)
+    if scales is None:
+        scales = torch.empty((k + 127) // 128, m, dtype=torch.float32, device=a.device)
+    _dev(q, torch.uint8, "q"); _dev(scales, torch.float32, "scales")
+    _check(load().fp8rl_quantize_act_gather(a.data_ptr(), m_src, k, a.stride(0), rows.data_ptr(),
+                                            m, q.data_ptr(), scales.data_ptr(), _stream(stream)))
+    return q, scales
+
+
+def silu_mul_quantize(h, q: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None,
+                      stream=None):
+    """h = [gate | up] BF16 [m, 2*inter] -> codes and group-major scales of
+    BF16(silu(gate) * up)."""
+    _dev(h, torch.bfloat16, "h")
+    _rowmajor(h, "h")
+    m, two_i = h.shape
+    if two_i % 2:
+        raise ValueError("h must have an even number of columns (gate | up)")
+    inter = two_i // 2
+    if q is None:
+        q = torch.empty(m, inter, dtype=torch.uint8, device=h.device)
+    if scales is None:
+        scales = torch.empty((inter + 127) // 128, m, dtype=torch.float32, device=h.device)
+    _dev(q, torch.uint8, "q"); _dev(scales, torch.float32, "scales")
+    _check(load().fp8rl_silu_mul_quantize(h.data_ptr(), m, inter, h.stride(0), q.data_ptr(),
+                                          scales.data_ptr(), _stream(stream)))
+    return q, scales
 
 
 # --------------------------------------------------------------------- TIS --

@@ -34,6 +34,7 @@ fp8rl_status device_state(DeviceState** out);
 // Device status word bits.
 enum : uint32_t {
   kStatusTimeout = 1u << 0,   // a pipelined kernel gave up on an mbarrier wait
+  kStatusBadIndex = 1u << 1,  // a device-side index was out of range (ignored)
 };
 
 // Encodes a 2-D tiled TMA descriptor over a row-major [rows, inner] matrix of

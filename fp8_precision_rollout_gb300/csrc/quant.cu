@@ -288,11 +288,16 @@ fp8rl_status check_wdesc(const fp8rl_wdesc& d, int idx) {
 // tasks may span rows and every lane has work even when kb is not a multiple
 // of 8.  4 lanes per group, each lane 4 x 16-byte chunks (chunk slot + 4i of
 // its group).  Scales go to the group-major array scales[g * m + r].
+// kGather: output row r is source row rows[r] of a (m_src rows); an index out
+// of range leaves the row zero and sets kStatusBadIndex.
+template <bool kGather>
 __global__ void __launch_bounds__(256) aquant_kernel(const uint16_t* __restrict__ a, int64_t m,
                                                      int64_t k, int64_t lda,
                                                      uint8_t* __restrict__ q,
                                                      float* __restrict__ scales,
-                                                     int64_t n_tasks, int kb) {
+                                                     int64_t n_tasks, int kb,
+                                                     const int32_t* __restrict__ rows,
+                                                     int64_t m_src, uint32_t* status) {
   const int lane = threadIdx.x & 31;
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -304,13 +309,22 @@ __global__ void __launch_bounds__(256) aquant_kernel(const uint16_t* __restrict_
     const int64_t r = valid ? f / kb : 0;
     const int g = (int)(f - r * kb);
     const int64_t gcol = (int64_t)g * 128;
-    const uint16_t* arow = a + r * lda;
+    int64_t src = r;
+    bool load = valid;
+    if (kGather && valid) {
+      src = __ldg(rows + r);
+      if (src < 0 || src >= m_src) {
+        load = false;
+        if (slot == 0 && g == 0) atomicOr(status, kStatusBadIndex);
+      }
+    }
+    const uint16_t* arow = a + (load ? src : 0) * lda;
     uint4 v[4];
     uint32_t m2 = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t col = gcol + (slot + 4 * i) * 8;
-      v[i] = (valid && col < k) ? ld_stream(arow + col) : make_uint4(0, 0, 0, 0);
+      v[i] = (load && col < k) ? ld_stream(arow + col) : make_uint4(0, 0, 0, 0);
       m2 = absmax8(m2, v[i]);
     }
     const float amax = warp_max(bf16x2_maxf(m2), 4);
@@ -322,6 +336,100 @@ __global__ void __launch_bounds__(256) aquant_kernel(const uint16_t* __restrict_
     for (int i = 0; i < 4; ++i) {
       const int64_t col = gcol + (slot + 4 * i) * 8;
       if (valid && col < k) *reinterpret_cast<uint2*>(qrow + col) = quant8_any<false>(v[i], sd);
+    }
+  }
+}
+
+// ------------------------------------------------------------- MoE glue --
+
+// The glue exponential E(x) (declared in fp8rl.h): Cody-Waite reduction by
+// ln2 with FMA, degree-7 Taylor polynomial in Horner form with FMA, exact
+// scaling by 2^k; one binary32 operation per step.
+__device__ __forceinline__ float glue_exp32(float x) {
+  if (x != x) return x;
+  if (x > 88.0f) return __int_as_float(0x7F800000);
+  if (x < -86.0f) return 0.0f;
+  const float kf = rintf(fx::fmul(x, 0x1.715476p+0f));
+  float r = fx::ffma(-kf, 0x1.62e43p-1f, x);
+  r = fx::ffma(-kf, -0x1.05c61p-29f, r);
+  float p = 0x1.a01a02p-13f;
+  p = fx::ffma(p, r, 0x1.6c16c2p-10f);
+  p = fx::ffma(p, r, 0x1.111112p-7f);
+  p = fx::ffma(p, r, 0x1.555556p-5f);
+  p = fx::ffma(p, r, 0x1.555556p-3f);
+  p = fx::ffma(p, r, 0.5f);
+  p = fx::ffma(p, r, 1.0f);
+  p = fx::ffma(p, r, 1.0f);
+  return fx::fmul(p, __int_as_float(((int)kf + 127) << 23));   // |k| <= 127: exact
+}
+
+// binary32 -> BF16 bits, round to nearest even (NaN stays a quiet NaN).
+__device__ __forceinline__ uint32_t bf16_rne_bits(float f) {
+  uint32_t b = __float_as_uint(f);
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return (b >> 16) | 0x0040u;
+  b += 0x7FFFu + ((b >> 16) & 1u);
+  return b >> 16;
+}
+
+// Two BF16 lanes (packed in a 32-bit word) of gate and up -> the packed BF16
+// pair silu(g) * u.
+__device__ __forceinline__ uint32_t silu_mul2(uint32_t g2, uint32_t u2) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float g = __uint_as_float((h ? (g2 >> 16) : (g2 & 0xFFFFu)) << 16);
+    const float u = __uint_as_float((h ? (u2 >> 16) : (u2 & 0xFFFFu)) << 16);
+    const float den = fx::fadd(1.0f, glue_exp32(-g));
+    const float y = fx::fmul(fx::fdiv(g, den), u);
+    out |= bf16_rne_bits(y) << (16 * h);
+  }
+  return out;
+}
+
+// Gated activation + 1x128 quantization: the task layout of aquant_kernel
+// over the [m, inter] output; each lane forms its 4 x 8 outputs from the
+// gate and up halves of its row, then quantizes them like aquant_kernel.
+__global__ void __launch_bounds__(256) silu_quant_kernel(const uint16_t* __restrict__ h, int64_t m,
+                                                         int64_t inter, int64_t ldh,
+                                                         uint8_t* __restrict__ q,
+                                                         float* __restrict__ scales,
+                                                         int64_t n_tasks, int kb) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int slot = lane & 3;
+  const int64_t groups = m * kb;
+  for (int64_t task = gw; task < n_tasks; task += nw) {
+    const int64_t f = task * 8 + (lane >> 2);
+    const bool valid = f < groups;
+    const int64_t r = valid ? f / kb : 0;
+    const int g = (int)(f - r * kb);
+    const int64_t gcol = (int64_t)g * 128;
+    const uint16_t* hrow = h + r * ldh;
+    uint4 v[4];
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t col = gcol + (slot + 4 * i) * 8;
+      if (valid && col < inter) {
+        const uint4 gv = ld_stream(hrow + col);
+        const uint4 uv = ld_stream(hrow + inter + col);
+        v[i] = make_uint4(silu_mul2(gv.x, uv.x), silu_mul2(gv.y, uv.y), silu_mul2(gv.z, uv.z),
+                          silu_mul2(gv.w, uv.w));
+      } else {
+        v[i] = make_uint4(0, 0, 0, 0);
+      }
+      m2 = absmax8(m2, v[i]);
+    }
+    const float amax = warp_max(bf16x2_maxf(m2), 4);
+    const float s = fx::fdiv(amax, 448.0f);
+    if (slot == 0 && valid) scales[(int64_t)g * m + r] = s;
+    const ScaleDiv sd = make_scale_div(s);
+    uint8_t* qrow = q + r * inter;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t col = gcol + (slot + 4 * i) * 8;
+      if (valid && col < inter) *reinterpret_cast<uint2*>(qrow + col) = quant8_any<false>(v[i], sd);
     }
   }
 }
@@ -487,10 +595,57 @@ extern "C" fp8rl_status fp8rl_quantize_act_groupwise(const void* a, int64_t m, i
   const int kb = (int)((k + 127) / 128);
   const int64_t tasks = (m * kb + 7) / 8;
   const int64_t ctas = (tasks + 7) / 8;
-  static const int per_sm = resident_ctas_per_sm(aquant_kernel, 256);
-  aquant_kernel<<<grid_for(ctas, ds, per_sm), 256, 0, stream>>>(
-      reinterpret_cast<const uint16_t*>(a), m, k, lda, q, scales, tasks, kb);
+  static const int per_sm = resident_ctas_per_sm(aquant_kernel<false>, 256);
+  aquant_kernel<false><<<grid_for(ctas, ds, per_sm), 256, 0, stream>>>(
+      reinterpret_cast<const uint16_t*>(a), m, k, lda, q, scales, tasks, kb, nullptr, m, ds->status);
   st = cuda_check(cudaGetLastError(), "aquant_kernel launch");
+  return st == FP8RL_OK ? ok() : st;
+}
+
+extern "C" fp8rl_status fp8rl_quantize_act_gather(const void* a, int64_t m_src, int64_t k,
+                                                  int64_t lda, const int32_t* rows, int64_t m,
+                                                  uint8_t* q, float* scales, cudaStream_t stream) {
+  if (m < 0 || m_src < 0 || k < 1 || lda < k)
+    return fail(FP8RL_ERR_INVALID_ARG, "need m, m_src >= 0, k >= 1 and lda >= k");
+  if (m == 0) return ok();
+  if (!a || !rows || !q || !scales) return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (k % 8 || lda % 8) return fail(FP8RL_ERR_ALIGNMENT, "k and lda must be multiples of 8");
+  if (!aligned(a, 16) || !aligned(q, 8) || !aligned(scales, 4) || !aligned(rows, 4))
+    return fail(FP8RL_ERR_ALIGNMENT, "a must be 16-byte, q 8-byte and rows 4-byte aligned");
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  if (st != FP8RL_OK) return st;
+  const int kb = (int)((k + 127) / 128);
+  const int64_t tasks = (m * kb + 7) / 8;
+  const int64_t ctas = (tasks + 7) / 8;
+  static const int per_sm = resident_ctas_per_sm(aquant_kernel<true>, 256);
+  aquant_kernel<true><<<grid_for(ctas, ds, per_sm), 256, 0, stream>>>(
+      reinterpret_cast<const uint16_t*>(a), m, k, lda, q, scales, tasks, kb, rows, m_src,
+      ds->status);
+  st = cuda_check(cudaGetLastError(), "aquant_kernel (gather) launch");
+  return st == FP8RL_OK ? ok() : st;
+}
+
+extern "C" fp8rl_status fp8rl_silu_mul_quantize(const void* h, int64_t m, int64_t inter,
+                                                int64_t ldh, uint8_t* q, float* scales,
+                                                cudaStream_t stream) {
+  if (m < 0 || inter < 1 || ldh < 2 * inter)
+    return fail(FP8RL_ERR_INVALID_ARG, "need m >= 0, inter >= 1 and ldh >= 2 * inter");
+  if (m == 0) return ok();
+  if (!h || !q || !scales) return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (inter % 8 || ldh % 8) return fail(FP8RL_ERR_ALIGNMENT, "inter and ldh must be multiples of 8");
+  if (!aligned(h, 16) || !aligned(q, 8) || !aligned(scales, 4))
+    return fail(FP8RL_ERR_ALIGNMENT, "h must be 16-byte and q 8-byte aligned");
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  if (st != FP8RL_OK) return st;
+  const int kb = (int)((inter + 127) / 128);
+  const int64_t tasks = (m * kb + 7) / 8;
+  const int64_t ctas = (tasks + 7) / 8;
+  static const int per_sm = resident_ctas_per_sm(silu_quant_kernel, 256);
+  silu_quant_kernel<<<grid_for(ctas, ds, per_sm), 256, 0, stream>>>(
+      reinterpret_cast<const uint16_t*>(h), m, inter, ldh, q, scales, tasks, kb);
+  st = cuda_check(cudaGetLastError(), "silu_quant_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }
 

@@ -133,5 +133,7 @@ extern "C" fp8rl_status fp8rl_device_status(int32_t device, int32_t clear) {
   if (st != FP8RL_OK) return st;
   if (words[0] & kStatusTimeout)
     return fail(FP8RL_ERR_TIMEOUT, "a kernel pipeline wait hit its time limit (site %u)", words[1]);
+  if (words[0] & kStatusBadIndex)
+    return fail(FP8RL_ERR_INVALID_ARG, "a device-side row index was out of range (row left zero)");
   return ok();
 }

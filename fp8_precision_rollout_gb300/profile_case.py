@@ -12,6 +12,8 @@ Cases (device footprint in parentheses):
   grouped         grouped W8A8 GEMM, Qwen3-30B-A3B gate_up, 128 experts (0.5 GB)
   kv              KV calibrate + quantize, 8 x 20480 tokens x 8 x 128 (0.5 GB)
   tis             TIS weights over 64 x 20480 tokens (0.02 GB)
+  glue_gather     MoE gather + quantize: 4096 tokens x 2048 -> 32768 routed rows (0.1 GB)
+  glue_silu       MoE SiLU(gate)*up + quantize: 32768 x 1536 -> 32768 x 768 (0.13 GB)
 """
 from __future__ import annotations
 
@@ -68,6 +70,14 @@ def main(argv=None):
     elif c == "tis":
         lt, lr = wl.tis_logprobs(64 * 20480, seed=5, device=dev, kind="student_t")
         run = lambda: fp8rl.tis_weights(lt, lr)  # noqa: E731
+    elif c == "glue_gather":
+        _, tok, _ = wl.moe_routing(seed=0)
+        x = wl.dense_acts(wl.MOE_TOKENS, wl.MOE_HIDDEN, seed=7, device=dev)
+        rows = tok.to(torch.int32).to(dev)
+        run = lambda: fp8rl.quantize_act_gather(x, rows)  # noqa: E731
+    elif c == "glue_silu":
+        h = wl.expert_inputs(wl.MOE_TOKENS * wl.MOE_TOPK, 2 * wl.MOE_INTER, seed=9, device=dev)
+        run = lambda: fp8rl.silu_mul_quantize(h)  # noqa: E731
     else:
         raise SystemExit("unknown case %r" % c)
     for _ in range(args.iters):

@@ -198,6 +198,40 @@ fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* logp_rollou
                                const uint8_t* mask, int64_t n, float c_hi, float c_lo, float* w,
                                cudaStream_t stream);
 
+/* MoE glue before the expert GEMMs: permute + quantize.  The expert-sorted
+ * activation matrix is the token matrix's rows a[rows[r]] (a token appears
+ * once per expert it is routed to; section 3.4.1 names the MoE expert layers
+ * among the quantized ones); each gathered row is quantized in 1x128 groups
+ * exactly as fp8rl_quantize_act_groupwise does.
+ *   a        BF16 [m_src, k] token matrix, row stride lda (>= k); k, lda
+ *            multiples of 8; 16-byte aligned
+ *   rows     int32 [m] (device), source row of each output row.  An index
+ *            outside [0, m_src) leaves that row's codes and scales zero and
+ *            sets a bit that fp8rl_device_status reports; nothing faults.
+ *   q        E4M3 [m, k] (row stride k), 8-byte aligned
+ *   scales   FP32 [ceil(k/128), m] group-major */
+fp8rl_status fp8rl_quantize_act_gather(const void* a, int64_t m_src, int64_t k, int64_t lda,
+                                       const int32_t* rows, int64_t m, uint8_t* q, float* scales,
+                                       cudaStream_t stream);
+
+/* MoE glue between the expert GEMMs: gated activation + quantize.  h holds
+ * the gate_up projection's output, gate in columns [0, inter) and up in
+ * [inter, 2*inter); y = BF16(silu(gate) * up) is quantized in 1x128 groups
+ * as fp8rl_quantize_act_groupwise does (the down projection's input).  The
+ * pages fix no activation arithmetic; the reading computed here, one
+ * binary32 operation per step: silu(g) = g / (1 + E(-g)), product with u,
+ * round to nearest even into BF16, where E is this exponential:
+ *   E(x) = +inf for x > 88, 0 for x < -86 (1 + E rounds to 1), NaN for NaN;
+ *   k = rint(fl32(x * RN(log2 e))); r = fma(-k, RN(ln2), x);
+ *   r = fma(-k, RN(ln2 - RN(ln2)), r); p = Horner with fma over the
+ *   binary32 roundings of 1/7!, 1/6!, ..., 1/2!, 1, 1; E = p * 2^k.
+ *   h        BF16 [m, 2*inter], row stride ldh (>= 2*inter); inter, ldh
+ *            multiples of 8; 16-byte aligned
+ *   q        E4M3 [m, inter] (row stride inter), 8-byte aligned
+ *   scales   FP32 [ceil(inter/128), m] group-major */
+fp8rl_status fp8rl_silu_mul_quantize(const void* h, int64_t m, int64_t inter, int64_t ldh,
+                                     uint8_t* q, float* scales, cudaStream_t stream);
+
 typedef enum fp8rl_is_mode {
   FP8RL_IS_TRUNCATE = 0,   /* TIS: w = min(e, c_hi), then max(w, c_lo) if c_lo > 0 */
   FP8RL_IS_MASK = 1        /* MIS: w = e if c_lo <= e <= c_hi, else 0 (NaN e: 0) */
@@ -231,8 +265,10 @@ fp8rl_status fp8rl_is_weights_stats(const float* logp_train, const float* logp_r
                                     int32_t mode, float* w, double* stats, cudaStream_t stream);
 
 /* Synchronizes the device and returns FP8RL_ERR_TIMEOUT if any kernel since
- * the last clear hit a device-side wait limit (FP8RL_OK otherwise); clears
- * the word when clear != 0.  device = CUDA ordinal. */
+ * the last clear hit a device-side wait limit, FP8RL_ERR_INVALID_ARG if a
+ * kernel met an out-of-range device-side index (fp8rl_quantize_act_gather),
+ * FP8RL_OK otherwise; clears the word when clear != 0.  device = CUDA
+ * ordinal. */
 fp8rl_status fp8rl_device_status(int32_t device, int32_t clear);
 
 #ifdef __cplusplus
