@@ -351,6 +351,60 @@ def tis_exp(logp_train, logp_rollout) -> np.ndarray:
 tis_exp.last_hard_count = 0
 
 
+def decode_attention_fp8kv(q, k_cache, v_cache, k_scale, v_scale, seq_lens, block_table=None,
+                           page: int = None, sm_scale: float = None):
+    """Decode attention over an FP8 E4M3 KV cache (summary page, section 3.4.4:
+    the cache stores K and V in FP8 with per-head scales; the FP8 pipeline's
+    attention reads them).  Plain float64 definition:
+
+      K[t] = dec(k_code[t]) * k_scale[h],  V[t] = dec(v_code[t]) * v_scale[h]
+      s_t  = sm_scale * <q, K[t]>,  p = softmax(s over t < len),  o = sum_t p_t V[t]
+
+    for every sequence s and query head hq, with KV head h = hq // (Hq / Hkv)
+    (grouped-query attention).  Token t of sequence s lives in page
+    block_table[s, t // page] at slot t % page; with block_table None the cache
+    is contiguous: page = its token dimension, sequence s in page s.
+      q        BF16 (or float) [S, Hq, D]
+      k_cache, v_cache  uint8 [pages, page, Hkv, D]
+      seq_lens int [S]
+    Returns float64 [S, Hq, D] (zeros for an empty context) and the float64
+    sum_t p_t |V[t]| [S, Hq, D] (the scale of the result, for tolerances)."""
+    import torch
+    qf = (q.float().numpy() if isinstance(q, torch.Tensor) else np.asarray(q)).astype(np.float64)
+    kc = np.asarray(k_cache, dtype=np.uint8)
+    vc = np.asarray(v_cache, dtype=np.uint8)
+    S, Hq, D = qf.shape
+    npages, pg, Hkv, _ = kc.shape
+    if page is None:
+        page = pg
+    group = Hq // Hkv
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    ks = np.asarray(k_scale, dtype=np.float32).astype(np.float64)
+    vs = np.asarray(v_scale, dtype=np.float32).astype(np.float64)
+    dec = e4m3_decode(np.arange(256, dtype=np.uint8))
+    out = np.zeros((S, Hq, D))
+    mag = np.zeros((S, Hq, D))
+    for si in range(S):
+        n = int(seq_lens[si])
+        if n <= 0:
+            continue
+        t = np.arange(n)
+        pages = (np.asarray(block_table)[si, t // page] if block_table is not None
+                 else np.full(n, si))
+        slot = t % page
+        for h in range(Hkv):
+            K = dec[kc[pages, slot, h, :]] * ks[h]            # [n, D]
+            V = dec[vc[pages, slot, h, :]] * vs[h]
+            for hq in range(h * group, (h + 1) * group):
+                sc = sm_scale * (K @ qf[si, hq])
+                e = np.exp(sc - sc.max())
+                p = e / e.sum()
+                out[si, hq] = p @ V
+                mag[si, hq] = p @ np.abs(V)
+    return out, mag
+
+
 IS_TRUNCATE, IS_MASK = 0, 1
 
 
