@@ -213,6 +213,11 @@ class Workload:
             x = wl.kv_tensor(seed=wl.sub_seed(6, t), device=dev)
             self.kv.append(dict(x=x, q=torch.empty(x.shape, dtype=torch.uint8, device=dev),
                                 s=torch.empty(8, dtype=torch.float32, device=dev)))
+        # decode attention of 32 query heads over the step's FP8 K and V caches
+        self.attn_q = torch.randn(64, 32, 128, generator=torch.Generator().manual_seed(7)).to(
+            torch.bfloat16).to(dev)
+        self.attn_lens = torch.full((64,), 20480, dtype=torch.int32, device=dev)
+        self.attn_out = torch.empty(64, 32, 128, dtype=torch.bfloat16, device=dev)
         self.lt, self.lr = wl.tis_logprobs(64 * 20480, seed=5, device=dev, kind="student_t")
         self.tw = torch.empty_like(self.lt)
         self.mw = torch.empty_like(self.lt)
@@ -259,6 +264,10 @@ class Workload:
             fp8rl.quantize_kv_fp8(t["x"], fp8rl.FP8RL_KV_CALIBRATE, t["s"], t["q"])
             launches += 2
         mark("kv_end")
+        fp8rl.decode_attention_fp8kv(self.attn_q, self.kv[0]["q"], self.kv[1]["q"], self.kv[0]["s"],
+                                     self.kv[1]["s"], self.attn_lens, out=self.attn_out)
+        launches += 1
+        mark("attn_end")
         fp8rl.tis_weights(self.lt, self.lr, None, 2.0, 0.0, self.tw)
         launches += 1
         mark("tis_end")
@@ -321,7 +330,12 @@ def _rows(W, ev, steps, peaks):
     kv_bytes = 5 * kv_elems            # calibrate pass reads 2 B, quantize reads 2 + writes 1
     out["a5_kv"] = {"ms": t, "bytes": kv_bytes, "gbs": kv_bytes / t / 1e6,
                     "frac_hbm": kv_bytes / t / 1e6 / hbm}
-    t = statistics.mean(_ms(ev, "kv_end", "tis_end"))
+    t = statistics.mean(_ms(ev, "kv_end", "attn_end"))
+    ab = 2 * W.kv[0]["q"].numel() + 2 * 2 * W.attn_q.numel()
+    out["a5b_decode_attention"] = {"ms": t, "bytes": ab, "gbs": ab / t / 1e6,
+                                   "frac_hbm": ab / t / 1e6 / hbm,
+                                   "shape": "64 seqs x 20480 tokens, 32 q heads over 8 FP8 KV heads"}
+    t = statistics.mean(_ms(ev, "attn_end", "tis_end"))
     tb = 12 * W.lt.numel()
     out["a6_tis"] = {"ms": t, "bytes": tb, "gbs": tb / t / 1e6, "frac_hbm": tb / t / 1e6 / hbm,
                      "note": "instruction-issue and launch bound at this size"}

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     FP8RL_KV_CALIBRATE,
     FP8RL_KV_GIVEN,
     Fp8rlError,
+    decode_attention_fp8kv,
     device_status,
     gemm_w8a8_blockwise,
     grouped_gemm_w8a8_blockwise,

@@ -70,6 +70,8 @@ def load(path: Optional[str] = None):
         "fp8rl_is_weights_stats": (ctypes.c_int, [P, P, P, i64, f32, f32, i32, P, P, P]),
         "fp8rl_quantize_act_gather": (ctypes.c_int, [P, i64, i64, i64, P, i64, P, P, P]),
         "fp8rl_silu_mul_quantize": (ctypes.c_int, [P, i64, i64, i64, P, P, P]),
+        "fp8rl_decode_attention_fp8kv": (ctypes.c_int, [P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                                        i32, i32, i32, f32, P, P]),
         "fp8rl_device_status": (ctypes.c_int, [i32, i32]),
     }
     for name, (res, args) in sigs.items():
@@ -274,6 +276,47 @@ def silu_mul_quantize(h, q: Optional[torch.Tensor] = None, scales: Optional[torc
     _check(load().fp8rl_silu_mul_quantize(h.data_ptr(), m, inter, h.stride(0), q.data_ptr(),
                                           scales.data_ptr(), _stream(stream)))
     return q, scales
+
+
+# -------------------------------------------------------------- attention --
+
+def decode_attention_fp8kv(q, k_cache, v_cache, k_scale, v_scale, seq_lens, block_table=None,
+                           sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                           stream=None):
+    """Decode attention of q BF16 [S, Hq, 128] over an E4M3 cache
+    [pages, page, Hkv, 128] (k_cache, v_cache, per-head scales [Hkv]).
+    block_table int32 [S, max_pages] or None (contiguous: the cache is
+    [S, T, Hkv, 128], or [S*T, Hkv, 128] rows as the KV quantizer writes)."""
+    _dev(q, torch.bfloat16, "q")
+    _dev(k_cache, torch.uint8, "k_cache"); _dev(v_cache, torch.uint8, "v_cache")
+    _dev(k_scale, torch.float32, "k_scale"); _dev(v_scale, torch.float32, "v_scale")
+    _dev(seq_lens, torch.int32, "seq_lens")
+    if not (q.is_contiguous() and k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("q and the caches must be contiguous")
+    if k_cache.shape != v_cache.shape or k_cache.dim() != 4:
+        raise ValueError("caches must be [pages, page, kv_heads, head_dim] and equal in shape")
+    S, hq, d = q.shape
+    pages, page, hkv, _ = k_cache.shape
+    if block_table is None:
+        if pages != S:
+            raise ValueError("a contiguous cache needs one page per sequence")
+        tp, max_pages = 0, 1
+    else:
+        _dev(block_table, torch.int32, "block_table")
+        if block_table.dim() != 2 or block_table.shape[0] != S or not block_table.is_contiguous():
+            raise ValueError("block_table must be a contiguous [S, max_pages] tensor")
+        tp, max_pages = block_table.data_ptr(), block_table.shape[1]
+    if out is None:
+        out = torch.empty(S, hq, d, dtype=torch.bfloat16, device=q.device)
+    _dev(out, torch.bfloat16, "out")
+    if sm_scale is None:
+        sm_scale = d ** -0.5
+    _check(load().fp8rl_decode_attention_fp8kv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                               k_scale.data_ptr(), v_scale.data_ptr(), tp,
+                                               seq_lens.data_ptr(), S, hq, hkv, d, page, max_pages,
+                                               pages, float(sm_scale), out.data_ptr(),
+                                               _stream(stream)))
+    return out
 
 
 # --------------------------------------------------------------------- TIS --

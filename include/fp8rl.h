@@ -232,6 +232,37 @@ fp8rl_status fp8rl_quantize_act_gather(const void* a, int64_t m_src, int64_t k, 
 fp8rl_status fp8rl_silu_mul_quantize(const void* h, int64_t m, int64_t inter, int64_t ldh,
                                      uint8_t* q, float* scales, cudaStream_t stream);
 
+/* Decode attention over an FP8 E4M3 KV cache (section 3.4.4: K and V are
+ * stored in E4M3 with per-head scales recalibrated every step; the decode
+ * step attends over that cache).  For every sequence s and query head hq,
+ * with KV head h = hq / (q_heads / kv_heads):
+ *   score_t = sm_scale * <q[s,hq], k_scale[h] * dec(K[s,t,h])>, t < seq_lens[s]
+ *   out[s,hq] = BF16(sum_t softmax(score)_t * v_scale[h] * dec(V[s,t,h]))
+ * computed in FP32 (an empty context gives zeros).  Token t of sequence s is
+ * slot t % page of page block_table[s * max_pages + t / page]; with
+ * block_table NULL, sequence s owns pages s*max_pages ... (a contiguous
+ * [num_seqs, max_pages*page, kv_heads, 128] cache, as fp8rl_quantize_kv_fp8
+ * writes it with rows = num_seqs * tokens).  Page indices outside
+ * [0, num_pages) are skipped and lengths above max_pages*page are clamped;
+ * both set the bit fp8rl_device_status reports.  Parity is within FP32
+ * rounding (accumulation order is the kernel's).
+ *   q          BF16 [num_seqs, q_heads, 128], 16-byte aligned
+ *   k_cache, v_cache  E4M3 [num_pages, page, kv_heads, 128], 16-byte aligned
+ *   k_scale, v_scale  FP32 [kv_heads] (device), the quantizer's scales
+ *   block_table int32 [num_seqs, max_pages] (device) or NULL
+ *   seq_lens   int32 [num_seqs] (device)
+ *   head_dim   must be 128; q_heads / kv_heads in {1, 2, 4, 8}
+ *   num_pages  pages in the pool (ignored when block_table is NULL)
+ *   sm_scale   softmax scale, typically 1/sqrt(128)
+ *   out        BF16 [num_seqs, q_heads, 128] */
+fp8rl_status fp8rl_decode_attention_fp8kv(const void* q, const uint8_t* k_cache,
+                                          const uint8_t* v_cache, const float* k_scale,
+                                          const float* v_scale, const int32_t* block_table,
+                                          const int32_t* seq_lens, int32_t num_seqs,
+                                          int32_t q_heads, int32_t kv_heads, int32_t head_dim,
+                                          int32_t page, int32_t max_pages, int32_t num_pages,
+                                          float sm_scale, void* out, cudaStream_t stream);
+
 typedef enum fp8rl_is_mode {
   FP8RL_IS_TRUNCATE = 0,   /* TIS: w = min(e, c_hi), then max(w, c_lo) if c_lo > 0 */
   FP8RL_IS_MASK = 1        /* MIS: w = e if c_lo <= e <= c_hi, else 0 (NaN e: 0) */
@@ -266,7 +297,8 @@ fp8rl_status fp8rl_is_weights_stats(const float* logp_train, const float* logp_r
 
 /* Synchronizes the device and returns FP8RL_ERR_TIMEOUT if any kernel since
  * the last clear hit a device-side wait limit, FP8RL_ERR_INVALID_ARG if a
- * kernel met an out-of-range device-side index (fp8rl_quantize_act_gather),
+ * kernel met an out-of-range device-side index (fp8rl_quantize_act_gather,
+ * fp8rl_decode_attention_fp8kv),
  * FP8RL_OK otherwise; clears the word when clear != 0.  device = CUDA
  * ordinal. */
 fp8rl_status fp8rl_device_status(int32_t device, int32_t clear);
