@@ -22,6 +22,7 @@ from .binding import (  # noqa: F401
     quantize_kv_fp8,
     quantize_weights_blockwise,
     quantize_weights_blockwise_multi,
+    quantize_weights_blockwise_multi_host,
     silu_mul_quantize,
     tis_weights,
     version,

@@ -69,6 +69,8 @@ def load(path: Optional[str] = None):
         "fp8rl_tis_weights": (ctypes.c_int, [P, P, P, i64, f32, f32, P, P]),
         "fp8rl_is_weights_stats": (ctypes.c_int, [P, P, P, i64, f32, f32, i32, P, P, P]),
         "fp8rl_quantize_act_gather": (ctypes.c_int, [P, i64, i64, i64, P, i64, P, P, P]),
+        "fp8rl_quantize_weights_blockwise_multi_host": (ctypes.c_int, [P, i32, P, ctypes.c_size_t,
+                                                                       P]),
         "fp8rl_silu_mul_quantize": (ctypes.c_int, [P, i64, i64, i64, P, P, P]),
         "fp8rl_decode_attention_fp8kv": (ctypes.c_int, [P, P, P, P, P, P, P, i32, i32, i32, i32,
                                                         i32, i32, i32, f32, P, P]),
@@ -234,6 +236,28 @@ def grouped_gemm_w8a8_blockwise(qa, sa, qw, sw, offsets, y: Optional[torch.Tenso
                                                     sw.data_ptr(), offsets.data_ptr(), e, m, n,
                                                     k, y.data_ptr(), _stream(stream)))
     return y
+
+
+def quantize_weights_blockwise_multi_host(ws, qs, ss, workspace: torch.Tensor, stream=None):
+    """Re-quantize HOST BF16 weights ws[i] [n, k] into HOST codes qs[i] and
+    scales ss[i], streaming through the device `workspace` (uint8 tensor);
+    copies and kernels overlap.  Host tensors should be pinned."""
+    if not (len(ws) == len(qs) == len(ss)):
+        raise ValueError("ws, qs and ss must have the same length")
+    _dev(workspace, torch.uint8, "workspace")
+    arr = (WDesc * max(len(ws), 1))()
+    for i, (w, q, s) in enumerate(zip(ws, qs, ss)):
+        for t, name, dt in ((w, "w", torch.bfloat16), (q, "q", torch.uint8), (s, "scales", torch.float32)):
+            if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != dt:
+                raise TypeError("%s[%d] must be a host %s tensor" % (name, i, dt))
+        _rowmajor(w, "w"); _rowmajor(q, "q")
+        if not s.is_contiguous():
+            raise ValueError("scales must be contiguous")
+        n, k = w.shape
+        arr[i] = WDesc(w.data_ptr(), q.data_ptr(), s.data_ptr(), n, k, w.stride(0), q.stride(0))
+    _check(load().fp8rl_quantize_weights_blockwise_multi_host(
+        ctypes.cast(arr, ctypes.c_void_p), len(ws), workspace.data_ptr(), workspace.numel(),
+        _stream(stream)))
 
 
 # --------------------------------------------------------------- MoE glue --

@@ -198,6 +198,29 @@ fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* logp_rollou
                                const uint8_t* mask, int64_t n, float c_hi, float c_lo, float* w,
                                cudaStream_t stream);
 
+/* Per-step re-quantization from and to HOST memory (section 3.4.2, Phase 2:
+ * the BF16 weights come from the training side, the E4M3 codes and scales go
+ * to the inference engine, every RL step).  Same results as
+ * fp8rl_quantize_weights_blockwise_multi, but each descriptor's w, q and
+ * scales are HOST pointers (page-locked memory lets the copies run
+ * asynchronously and overlap; pageable memory works but serializes them).
+ * The tensors stream through `workspace` (DEVICE, 256-byte aligned, owned by
+ * the caller, at least 2 x the bytes of 128 rows of the widest tensor,
+ * 3 bytes per element plus scales; tens to hundreds of MB keep the copies
+ * and the kernels overlapped): the host-to-device copy of one chunk, the
+ * quantization of the previous one and the device-to-host copy of the one
+ * before run together on internal streams; tensors larger than half the
+ * workspace are split at 128-row boundaries.  Nothing is allocated.
+ * Stream-ordered: starts after earlier work on `stream`, and `stream` waits
+ * for the last copy; the host buffers must stay valid until then.  Calls on
+ * one device are serialized on the library's internal streams.
+ *   descs    HOST array of count descriptors (w, q, scales in host memory;
+ *            k a multiple of 8, ldw >= k, ldq >= k)
+ *   workspace, workspace_bytes  the device staging buffer */
+fp8rl_status fp8rl_quantize_weights_blockwise_multi_host(const fp8rl_wdesc* descs, int32_t count,
+                                                         void* workspace, size_t workspace_bytes,
+                                                         cudaStream_t stream);
+
 /* MoE glue before the expert GEMMs: permute + quantize.  The expert-sorted
  * activation matrix is the token matrix's rows a[rows[r]] (a token appears
  * once per expert it is routed to; section 3.4.1 names the MoE expert layers

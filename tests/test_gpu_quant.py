@@ -217,3 +217,30 @@ def test_kv_long_context_full_size():
     assert (qr == oracle.kv_quantize(xr_cpu[torch.from_numpy(rows)], os_)).all()
     del x, q, xr_cpu
     torch.cuda.empty_cache()
+
+
+def test_host_streaming_requant_matches_device_path():
+    """Host BF16 in, host codes and scales out, through a workspace small enough
+    to split tensors across chunks; bit-identical to the device multi-tensor path."""
+    dev = device()
+    shapes = [(1000, 512), (128, 136), (300, 2048), (7, 8), (640, 1024)]
+    ws = [workloads.make_weight(n, k, seed=70 + i) for i, (n, k) in enumerate(shapes)]
+    # strided host rows for one tensor (ldw > k, ldq > k)
+    big = torch.zeros(300, 2048 + 64, dtype=torch.bfloat16)
+    big[:, :2048] = ws[2]
+    hw = [w.pin_memory() for w in ws]
+    hw[2] = big.pin_memory()[:, :2048]
+    qbig = torch.full((300, 2048 + 32), 0x5A, dtype=torch.uint8).pin_memory()
+    hq = [torch.empty(w.shape, dtype=torch.uint8).pin_memory() for w in ws]
+    hq[2] = qbig[:, :2048]
+    hs = [torch.empty((w.shape[0] + 127) // 128, (w.shape[1] + 127) // 128,
+                      dtype=torch.float32).pin_memory() for w in ws]
+    work = torch.empty(2 * 1_300_000, dtype=torch.uint8, device=dev)       # ~430 rows of k = 1024 per half
+    fp8rl.quantize_weights_blockwise_multi_host(hw, hq, hs, work)
+    torch.cuda.synchronize()
+    fp8rl.device_status(0)
+    qd, sd = fp8rl.quantize_weights_blockwise_multi([w.to(dev) for w in ws])
+    for i in range(len(ws)):
+        assert (hq[i].numpy() == qd[i].cpu().numpy()).all(), i
+        assert (hs[i].numpy().view(np.uint32) == sd[i].cpu().numpy().view(np.uint32)).all(), i
+    assert (qbig[:, 2048:].numpy() == 0x5A).all()         # row padding untouched
