@@ -8,16 +8,31 @@
 //   o   = sum_t p_t * v_scale[h] * dec(V[t]),      out = BF16(o).
 // Token t of sequence s lives in page block_table[s][t / page], slot t % page.
 //
-// One CTA per (sequence, KV head): a producer warp TMA-loads the head's
-// 128-byte slice of 64 consecutive tokens of K and of V per stage (16 KB)
-// into a 4-stage mbarrier ring, with the stage's valid-token mask; 4 consumer
-// warps run 8 token streams of 16 lanes (lane j holds dimensions [8j, 8j+8)
-// for all G query heads of the group, so each byte is used for the G heads),
-// stream k taking the stage's tokens [8k, 8k+8).  Online softmax in the log2
-// domain (q pre-multiplied by sm_scale * k_scale * log2 e), rescaled once per
-// 8-token block; the 8 streams are combined through shared memory at the end.
-// Codes are dequantized with the hardware e4m3x2 -> f16x2 conversion (exact:
-// every E4M3 value is an FP16 value).  Every mbarrier wait is bounded.
+// One CTA per (sequence, KV head).  A producer warp TMA-loads the head's
+// 128-byte slice of 64 consecutive tokens of K and of V per stage (16 KB, in
+// the 128-byte swizzled layout when the boxes allow it) into a 6-slot
+// mbarrier ring, with the stage's valid-token mask; its lanes look up the
+// pages of a stage's boxes together, one stage ahead.  Three consumer warps
+// take whole stages in turn, warp w the stages i with i % 3 == w, so that a
+// slot (i % 6) always has the same consumer, which waits on its barrier in
+// order (a warp can never wait on a slot whose previous phase another warp
+// has not consumed yet).  Both contractions of a stage run on the tensor cores as
+// m16n8k16 FP16 MMAs with FP32 accumulation, the G <= 8 query heads of the
+// group on the n = 8 side:
+//   scores  S[16 tokens x 8 heads]   += K[16 tokens x 16 dims] * Q^T[16 dims x 8]
+//   output  O^T[16 dims x 8 heads]   += V^T[16 dims x 16 tokens] * P^T[16 tokens x 8]
+// The operands of the first product are exact: every E4M3 code is an FP16
+// value (hardware e4m3x2 -> f16x2 conversion), and q is scaled per head by a
+// power of two into [2^14, 2^15) before its FP16 conversion, the factor
+// folded back into the score scale.  The probabilities, scaled by 2^15 so
+// that FP16 keeps them normal down to 2^-29, are rounded to FP16 for the
+// second product; the normaliser sums them in FP32.  The order of the
+// dimensions inside a k-step, and of the output rows, are permutations chosen
+// so that every lane reads whole 16-byte chunks; the score fragment becomes
+// the second product's operand through an in-register transpose (movmatrix).
+// Online softmax in the log2 domain, rescaled once per stage; the three warps
+// are combined through shared memory at the end.  Every mbarrier wait is
+// bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -34,16 +49,16 @@ namespace {
 using namespace ptx;
 
 constexpr int kHeadDim = 128;
-constexpr int kLanesPerToken = 16;
-constexpr int kDimsPerLane = kHeadDim / kLanesPerToken;          // 8
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 3;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;          // + producer warp
-constexpr int kStreams = kConsumerWarps * 32 / kLanesPerToken;   // 8
-constexpr int kBlk = 8;                                          // tokens per stream per stage
-constexpr int kStageTokens = kStreams * kBlk;                    // 64
-constexpr int kStages = 4;
+constexpr int kStageTokens = 64;
+constexpr int kMTiles = kStageTokens / 16;                       // 16-token MMA tiles per stage
+constexpr int kStages = 6;
 constexpr int kHalfStage = kStageTokens * kHeadDim;              // K (or V) of a stage: 8 KB
 constexpr int kStageBytes = 2 * kHalfStage;
+constexpr int kMaxG = 8;                                         // the MMA's n
+constexpr float kPScale = 32768.0f;   // probabilities enter the FP16 product as p * 2^15
+static_assert(kStages % kConsumerWarps == 0, "a ring slot must always have the same consumer warp");
 
 struct AttnShared {
   uint64_t full[kStages];
@@ -52,6 +67,9 @@ struct AttnShared {
   uint32_t abort_flag;
 };
 constexpr size_t kAttnSmem = 1024 + (size_t)kStages * kStageBytes + sizeof(AttnShared);
+static_assert((size_t)kConsumerWarps * (2 + kHeadDim) * kMaxG * sizeof(float) <=
+                  (size_t)kStages * kStageBytes,
+              "the combine buffers must fit in the idle stages");
 
 // 2^x with the hardware approximation (relative error about 2^-22); the
 // attention is compared with a tolerance, not bit for bit.
@@ -61,18 +79,45 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Four E4M3 codes (one 32-bit word) -> four floats, exactly.
-__device__ __forceinline__ void dec4(uint32_t w, float* f) {
-  uint32_t lo, hi;
+// Four E4M3 codes (one 32-bit word, byte i = element i) -> two f16x2: lo
+// holds elements (0, 1), hi holds (2, 3), the lower index in the lower half.
+__device__ __forceinline__ void dec_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   asm("{\n\t.reg .b16 a, b;\n\t"
       "mov.b32 {a, b}, %2;\n\t"
       "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
       "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
       : "=r"(lo), "=r"(hi)
       : "r"(w));
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+
+// D += A * B, m16n8k16, FP16 operands, FP32 accumulation.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of the warp's 8x8 matrix of 16-bit values (lane l holds row l/4,
+// columns 2(l%4) and 2(l%4)+1).
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* a) {
+  return *reinterpret_cast<const uint4*>(a);
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
 struct AttnParams {
@@ -82,7 +127,7 @@ struct AttnParams {
   const int32_t* table;       // [S, max_pages] or null: page of (s, j) = s * max_pages + j
   const int32_t* lens;        // [S]
   __nv_bfloat16* out;         // [S, Hq, 128]
-  int S, Hq, Hkv, page, max_pages, num_pages;
+  int S, Hq, Hkv, G, page, max_pages, num_pages;
   int boxr;                   // rows per TMA box (divides page when paged; 64 if contiguous)
   float sm_scale_log2;        // sm_scale * log2(e)
   uint32_t* status;
@@ -105,7 +150,9 @@ __device__ __forceinline__ int token_row(const AttnParams& p, int s, int t, int 
   return pg * p.page + slot;
 }
 
-template <int G>
+// kSwz: the stage rows are in the 128-byte swizzled layout (16-byte chunk j
+// of row r stored at chunk j ^ (r % 8)); otherwise plain 128-byte rows.
+template <bool kSwz>
 __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const AttnParams p) {
@@ -115,6 +162,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
   AttnShared* sh = reinterpret_cast<AttnShared*>(smem + kStages * kStageBytes);
   volatile uint32_t* abort_flag = &sh->abort_flag;
   const int s = blockIdx.x / p.Hkv, h = blockIdx.x % p.Hkv;
+  const int G = p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int len = __ldg(p.lens + s);
   const int cap = p.max_pages * p.page;
@@ -126,7 +174,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&sh->full[i]), 1);
-      mbar_init(smem_u32(&sh->empty[i]), kConsumerWarps);
+      mbar_init(smem_u32(&sh->empty[i]), 1);
     }
     sh->abort_flag = 0;
     mbar_fence_init();
@@ -135,193 +183,309 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
   }
   __syncthreads();
 
-  float m[G], l[G], o[G][kDimsPerLane];
-  const int stream = (tid & 127) / kLanesPerToken;   // consumers: 0..7
-  const int j = lane & (kLanesPerToken - 1);         // dimension slice
+  // consumer lane (g, c) = (lane / 4, lane % 4) keeps the state of heads 2c, 2c+1
+  const int g = lane >> 2, c = lane & 3;
+  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+  float o[8][4];
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer --
-    if (lane == 0) {
-      uint32_t issued = 0;
-      bool any_bad = false;
-      for (int i = 0; i < nst; ++i) {
-        const int st = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (!mbar_wait(smem_u32(&sh->empty[st]), ph ^ 1u, abort_flag, p.status, 31)) break;
-        uint64_t mask = 0;
-        for (int r = 0; r < kStageTokens; r += p.boxr) {
+    // lane l handles boxes l and l + 32 of a stage (64 / boxr boxes)
+    const int nbox = kStageTokens / p.boxr;
+    int row[2] = {0, 0}, vrows[2] = {0, 0};
+    bool bad_seen = false;
+    auto lookup = [&](int i) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int b = lane + 32 * u;
+        row[u] = 0;
+        vrows[u] = 0;
+        if (b < nbox) {
           bool ok, bad;
-          token_row(p, s, i * kStageTokens + r, len, ok, bad);
-          any_bad |= bad;
-          if (ok) {
-            const int valid_rows = min(p.boxr, len - (i * kStageTokens + r));
-            mask |= ((valid_rows >= 64 ? ~0ull : ((1ull << valid_rows) - 1ull)) << r);
-          }
+          const int t = i * kStageTokens + b * p.boxr;
+          row[u] = token_row(p, s, t, len, ok, bad);
+          bad_seen |= bad;
+          if (ok) vrows[u] = min(p.boxr, len - t);
         }
-        sh->vmask[st] = mask;
-        const uint32_t fb = smem_u32(&sh->full[st]);
-        mbar_expect_tx(fb, kStageBytes);   // arrives; the mask store above is released with it
-        uint8_t* kdst = smem + st * kStageBytes;
-        for (int r = 0; r < kStageTokens; r += p.boxr) {
-          bool ok, bad;
-          const int row = token_row(p, s, i * kStageTokens + r, len, ok, bad);
-          tma_load_2d(smem_u32(kdst + r * kHeadDim), &tmK, fb, h * kHeadDim, row);
-          tma_load_2d(smem_u32(kdst + kHalfStage + r * kHeadDim), &tmV, fb, h * kHeadDim, row);
-        }
-        ++issued;
       }
-      if (any_bad) atomicOr(p.status, kStatusBadIndex);
-      if (issued < (uint32_t)nst) {
-        // gave up: let the stages still in flight land before the CTA moves on
-        const uint32_t n = issued < (uint32_t)kStages ? issued : (uint32_t)kStages;
-        for (uint32_t k = 1; k <= n; ++k) {
-          const uint32_t i2 = issued - k;
-          mbar_drain(smem_u32(&sh->full[i2 % kStages]), (i2 / kStages) & 1u, p.status, 33);
+    };
+    if (nst > 0) lookup(0);
+    uint32_t issued = 0;
+    for (int i = 0; i < nst; ++i) {
+      const int st = i % kStages;
+      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      bool okw = true;
+      if (lane == 0) okw = mbar_wait(smem_u32(&sh->empty[st]), ph ^ 1u, abort_flag, p.status, 31);
+      if (!__shfl_sync(0xFFFFFFFFu, okw ? 1 : 0, 0)) break;
+      uint64_t mask = 0;
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        if (vrows[u] > 0)
+          mask |= (vrows[u] >= 64 ? ~0ull : ((1ull << vrows[u]) - 1ull)) << ((lane + 32 * u) * p.boxr);
+      const uint32_t mlo = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)mask);
+      const uint32_t mhi = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)(mask >> 32));
+      const uint32_t fb = smem_u32(&sh->full[st]);
+      if (lane == 0) {
+        sh->vmask[st] = ((uint64_t)mhi << 32) | mlo;
+        mbar_expect_tx(fb, kStageBytes);   // arrives; the mask store above is released with it
+      }
+      __syncwarp();
+      uint8_t* kdst = smem + st * kStageBytes;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int b = lane + 32 * u;
+        if (b < nbox) {
+          tma_load_2d(smem_u32(kdst + b * p.boxr * kHeadDim), &tmK, fb, h * kHeadDim, row[u]);
+          tma_load_2d(smem_u32(kdst + kHalfStage + b * p.boxr * kHeadDim), &tmV, fb, h * kHeadDim,
+                      row[u]);
         }
+      }
+      ++issued;
+      if (i + 1 < nst) lookup(i + 1);   // the page-table loads overlap the next wait
+    }
+    if (__any_sync(0xFFFFFFFFu, bad_seen) && lane == 0) atomicOr(p.status, kStatusBadIndex);
+    if (lane == 0 && issued < (uint32_t)nst) {
+      // gave up: let the stages still in flight land before the CTA moves on
+      const uint32_t n = issued < (uint32_t)kStages ? issued : (uint32_t)kStages;
+      for (uint32_t k = 1; k <= n; ++k) {
+        const uint32_t i2 = issued - k;
+        mbar_drain(smem_u32(&sh->full[i2 % kStages]), (i2 / kStages) & 1u, p.status, 33);
       }
     }
     __syncwarp();
   } else {
     // ----------------------------------------------------------- consumers --
-    const float kscale = __ldg(p.k_scale + h) * p.sm_scale_log2;
-    float q[G][kDimsPerLane];
+    // Q as the first product's B operand: lane (g, c) holds head g,
+    // dimensions [32c, 32c + 32), k-step j taking [32c + 4j, 32c + 4j + 4)
+    // (zero for g >= G).  Head g is scaled by 2^e_g, max |q| in [2^14, 2^15).
+    uint32_t qb[8][2];
+    int e = 0;
+    {
+      float qf[32];
+      float amax = 0.f;
+      const bool real = g < G;
+      const __nv_bfloat16* qrow = p.q + ((size_t)s * p.Hq + h * G + (real ? g : 0)) * kHeadDim;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(
-          p.q + ((size_t)s * p.Hq + h * G + g) * kHeadDim + j * kDimsPerLane);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      for (int u = 0; u < 4; ++u) {
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (real) raw = *reinterpret_cast<const uint4*>(qrow + 32 * c + 8 * u);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(b2[i]);
-        q[g][2 * i] = f.x * kscale;
-        q[g][2 * i + 1] = f.y * kscale;
+        for (int v = 0; v < 4; ++v) {
+          const float2 f = __bfloat1622float2(b2[v]);
+          qf[8 * u + 2 * v] = f.x;
+          qf[8 * u + 2 * v + 1] = f.y;
+          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+      // e = 14 - floor(log2 max|q|), kept within [-100, 100]; zero heads: e = 0
+      if (amax > 0.f) {
+        const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
+        e = min(max(14 - ex, -100), 100);
+      }
+      const float up = __int_as_float((uint32_t)(127 + e) << 23);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        qb[j][0] = pack_f16x2(qf[4 * j] * up, qf[4 * j + 1] * up);
+        qb[j][1] = pack_f16x2(qf[4 * j + 2] * up, qf[4 * j + 3] * up);
       }
     }
+    // score factor of head n: sm_scale * log2(e) * k_scale * 2^-e_n; lane
+    // (g, c) needs heads 2c and 2c+1, whose exponents the lanes g = 2c, 2c+1 hold
+    const float base = p.sm_scale_log2 * __ldg(p.k_scale + h);
+    const int eA = __shfl_sync(0xFFFFFFFFu, e, (2 * c) * 4);
+    const int eB = __shfl_sync(0xFFFFFFFFu, e, (2 * c + 1) * 4);
+    const float fA = base * __int_as_float((uint32_t)(127 - eA) << 23);
+    const float fB = base * __int_as_float((uint32_t)(127 - eB) << 23);
+
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m[g] = -INFINITY;
-      l[g] = 0.f;
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int i = 0; i < kDimsPerLane; ++i) o[g][i] = 0.f;
-    }
-    // every consumer lane runs all nst stages (a CTA-uniform count), so every
-    // lane reaches every full-warp shuffle
-    for (int i = 0; i < nst; ++i) {
+      for (int r = 0; r < 4; ++r) o[i][r] = 0.f;
+
+    // byte offsets of this lane's 16-byte chunks within a row; every MMA tile
+    // starts at a multiple of 8 rows, so a row's swizzle term is known here
+    const uint32_t kofs0 = (uint32_t)(((2 * c) ^ (kSwz ? g : 0)) << 4);       // K rows g, g+8
+    const uint32_t kofs1 = (uint32_t)(((2 * c + 1) ^ (kSwz ? g : 0)) << 4);
+    const uint32_t vofs0 = (uint32_t)((g ^ (kSwz ? 2 * c : 0)) << 4);         // V rows 2c, 2c+8
+    const uint32_t vofs1 = (uint32_t)((g ^ (kSwz ? 2 * c + 1 : 0)) << 4);     // V rows 2c+1, 2c+9
+
+    // warp w takes stages w, w+3, ...: a warp-uniform count, so every lane
+    // reaches every full-warp shuffle, MMA and transpose
+    for (int i = warp; i < nst; i += kConsumerWarps) {
       const int st = i % kStages;
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
       bool okw = mbar_wait(smem_u32(&sh->full[st]), ph, abort_flag, p.status, 32);
       okw = __all_sync(0xFFFFFFFFu, okw);
       if (!okw) break;
       const uint64_t vm = sh->vmask[st];
+      const bool all_valid = vm == ~0ull;
       const uint8_t* ks = smem + st * kStageBytes;
-      uint2 kw[kBlk], vw[kBlk];
-      bool val[kBlk];
+      const uint8_t* vs = ks + kHalfStage;
+
+      // scores of the stage's four 16-token tiles, in the log2 domain
+      float sc[kMTiles][4];
 #pragma unroll
-      for (int u = 0; u < kBlk; ++u) {
-        const int r = stream * kBlk + u;
-        val[u] = (vm >> r) & 1ull;
-        kw[u] = *reinterpret_cast<const uint2*>(ks + r * kHeadDim + j * kDimsPerLane);
-        vw[u] = *reinterpret_cast<const uint2*>(ks + kHalfStage + r * kHeadDim + j * kDimsPerLane);
+      for (int mt = 0; mt < kMTiles; ++mt) {
+        const uint8_t* r0 = ks + (mt * 16 + g) * kHeadDim;
+        const uint8_t* r1 = r0 + 8 * kHeadDim;
+        const uint4 ka0 = lds128(r0 + kofs0), ka1 = lds128(r0 + kofs1);
+        const uint4 kb0 = lds128(r1 + kofs0), kb1 = lds128(r1 + kofs1);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t alo, ahi, blo, bhi;
+          dec_f16x2(word(j < 4 ? ka0 : ka1, j & 3), alo, ahi);
+          dec_f16x2(word(j < 4 ? kb0 : kb1, j & 3), blo, bhi);
+          mma_f16(d, alo, blo, ahi, bhi, qb[j][0], qb[j][1]);
+        }
+        const bool v0 = all_valid || ((vm >> (mt * 16 + g)) & 1ull);
+        const bool v1 = all_valid || ((vm >> (mt * 16 + g + 8)) & 1ull);
+        sc[mt][0] = v0 ? d[0] * fA : -INFINITY;
+        sc[mt][1] = v0 ? d[1] * fB : -INFINITY;
+        sc[mt][2] = v1 ? d[2] * fA : -INFINITY;
+        sc[mt][3] = v1 ? d[3] * fB : -INFINITY;
+      }
+      // stage maxima of heads 2c, 2c+1 (over the lanes with this c)
+      float xA = -INFINITY, xB = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < kMTiles; ++mt) {
+        xA = fmaxf(xA, fmaxf(sc[mt][0], sc[mt][2]));
+        xB = fmaxf(xB, fmaxf(sc[mt][1], sc[mt][3]));
+      }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        xA = fmaxf(xA, __shfl_xor_sync(0xFFFFFFFFu, xA, off));
+        xB = fmaxf(xB, __shfl_xor_sync(0xFFFFFFFFu, xB, off));
+      }
+      const float nA = fmaxf(mA, xA), nB = fmaxf(mB, xB);
+      const float uA = nA == -INFINITY ? 0.f : nA, uB = nB == -INFINITY ? 0.f : nB;
+      const float cA = ex2(mA - uA), cB = ex2(mB - uB);   // 0 while nothing valid was seen
+      mA = nA;
+      mB = nB;
+      lA *= cA;
+      lB *= cB;
+#pragma unroll
+      for (int i2 = 0; i2 < 8; ++i2) {
+        o[i2][0] *= cA;
+        o[i2][1] *= cB;
+        o[i2][2] *= cA;
+        o[i2][3] *= cB;
+      }
+      // probabilities, then the B operands of the second product
+      uint32_t pb[kMTiles][2];
+#pragma unroll
+      for (int mt = 0; mt < kMTiles; ++mt) {
+        const float p0 = ex2(sc[mt][0] - uA), p1 = ex2(sc[mt][1] - uB);
+        const float p2 = ex2(sc[mt][2] - uA), p3 = ex2(sc[mt][3] - uB);
+        lA += p0 + p2;
+        lB += p1 + p3;
+        // x 2^15: p down to 2^-29 stays a normal FP16 number (undone at the end)
+        pb[mt][0] = transpose8x8(pack_f16x2(p0 * kPScale, p1 * kPScale));   // tokens 2c, 2c+1, head g
+        pb[mt][1] = transpose8x8(pack_f16x2(p2 * kPScale, p3 * kPScale));   // tokens 2c+8, 2c+9
+      }
+      // O^T += V^T P^T.  Row g of output tile i is dimension 16g + 2i, row
+      // g+8 is 16g + 2i + 1; the k index is the tile's token order.
+#pragma unroll
+      for (int mt = 0; mt < kMTiles; ++mt) {
+        const int t0 = mt * 16 + 2 * c;
+        uint4 x0 = lds128(vs + t0 * kHeadDim + vofs0);
+        uint4 x1 = lds128(vs + (t0 + 1) * kHeadDim + vofs1);
+        uint4 x2 = lds128(vs + (t0 + 8) * kHeadDim + vofs0);
+        uint4 x3 = lds128(vs + (t0 + 9) * kHeadDim + vofs1);
+        if (!all_valid) {
+          // an invalid row holds a copy of pool row 0; its p is 0, and its
+          // codes are zeroed so that no NaN code can reach the sum
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          if (!((vm >> t0) & 1ull)) x0 = z;
+          if (!((vm >> (t0 + 1)) & 1ull)) x1 = z;
+          if (!((vm >> (t0 + 8)) & 1ull)) x2 = z;
+          if (!((vm >> (t0 + 9)) & 1ull)) x3 = z;
+        }
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+#pragma unroll
+          for (int hs = 0; hs < 2; ++hs) {
+            // bytes 2hs, 2hs+1 of word w: dimensions 16g + 4w + 2hs (+1)
+            const uint32_t sel = hs ? 0x7362u : 0x5140u;
+            uint32_t a0, a1, a2, a3;
+            dec_f16x2(__byte_perm(word(x0, w), word(x1, w), sel), a0, a1);
+            dec_f16x2(__byte_perm(word(x2, w), word(x3, w), sel), a2, a3);
+            mma_f16(o[2 * w + hs], a0, a1, a2, a3, pb[mt][0], pb[mt][1]);
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh->empty[st]));
-      float sc[kBlk][G];
+    }
 #pragma unroll
-      for (int u = 0; u < kBlk; ++u) {
-        float kf[8];
-        dec4(kw[u].x, kf);
-        dec4(kw[u].y, kf + 4);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float a = 0.f;
-#pragma unroll
-          for (int d = 0; d < kDimsPerLane; ++d) a = fmaf(q[g][d], kf[d], a);
-          sc[u][g] = a;
-        }
-      }
-#pragma unroll
-      for (int off2 = kLanesPerToken / 2; off2 > 0; off2 >>= 1) {
-#pragma unroll
-        for (int u = 0; u < kBlk; ++u)
-#pragma unroll
-          for (int g = 0; g < G; ++g) sc[u][g] += __shfl_xor_sync(0xFFFFFFFFu, sc[u][g], off2);
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float bm = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < kBlk; ++u)
-          if (val[u]) bm = fmaxf(bm, sc[u][g]);
-        if (bm == -INFINITY) continue;           // nothing valid for this stream here
-        const float mn = fmaxf(m[g], bm);
-        const float corr = ex2(m[g] - mn);       // 0 on the first block (m = -inf)
-        l[g] *= corr;
-#pragma unroll
-        for (int d = 0; d < kDimsPerLane; ++d) o[g][d] *= corr;
-        m[g] = mn;
-      }
-#pragma unroll
-      for (int u = 0; u < kBlk; ++u) {
-        if (!val[u]) continue;
-        float vf[8];
-        dec4(vw[u].x, vf);
-        dec4(vw[u].y, vf + 4);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float pr = ex2(sc[u][g] - m[g]);
-          l[g] += pr;
-#pragma unroll
-          for (int d = 0; d < kDimsPerLane; ++d) o[g][d] = fmaf(pr, vf[d], o[g][d]);
-        }
-      }
+    for (int off = 4; off < 32; off <<= 1) {
+      lA += __shfl_xor_sync(0xFFFFFFFFu, lA, off);
+      lB += __shfl_xor_sync(0xFFFFFFFFu, lB, off);
     }
   }
-  // ---------------------------------------------- combine the 8 streams --
+  // ------------------------------------------------ combine the 3 warps --
   // (the stage buffers are idle now: every issued stage was consumed, or
   // drained by the producer after a timeout)
   __syncthreads();
-  float* cm = reinterpret_cast<float*>(smem);            // [kStreams][G]
-  float* cl = cm + kStreams * G;                         // [kStreams][G]
-  float* co = cl + kStreams * G;                         // [kStreams][G][128]
+  float* cm = reinterpret_cast<float*>(smem);            // [kConsumerWarps][G]
+  float* cl = cm + kConsumerWarps * G;                   // [kConsumerWarps][G]
+  float* co = cl + kConsumerWarps * G;                   // [kConsumerWarps][G][128]
   if (warp < kConsumerWarps) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (j == 0) {
-        cm[stream * G + g] = m[g];
-        cl[stream * G + g] = l[g];
+    const int hA = 2 * c, hB = 2 * c + 1;
+    if (g == 0) {
+      if (hA < G) {
+        cm[warp * G + hA] = mA;
+        cl[warp * G + hA] = lA;
       }
+      if (hB < G) {
+        cm[warp * G + hB] = mB;
+        cl[warp * G + hB] = lB;
+      }
+    }
 #pragma unroll
-      for (int d = 0; d < kDimsPerLane; ++d)
-        co[(stream * G + g) * kHeadDim + j * kDimsPerLane + d] = o[g][d];
+    for (int i = 0; i < 8; ++i) {
+      const int d0 = 16 * g + 2 * i;
+      const float un = 1.0f / kPScale;   // exact
+      if (hA < G) {
+        co[(warp * G + hA) * kHeadDim + d0] = o[i][0] * un;
+        co[(warp * G + hA) * kHeadDim + d0 + 1] = o[i][2] * un;
+      }
+      if (hB < G) {
+        co[(warp * G + hB) * kHeadDim + d0] = o[i][1] * un;
+        co[(warp * G + hB) * kHeadDim + d0 + 1] = o[i][3] * un;
+      }
     }
   }
   __syncthreads();
   const float vscale = __ldg(p.v_scale + h);
   for (int idx = tid; idx < G * kHeadDim; idx += kAttnThreads) {
-    const int g = idx / kHeadDim, d = idx - g * kHeadDim;
+    const int n = idx / kHeadDim, d = idx - n * kHeadDim;
     float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kStreams; ++k) M = fmaxf(M, cm[k * G + g]);
+    for (int k = 0; k < kConsumerWarps; ++k) M = fmaxf(M, cm[k * G + n]);
     float L = 0.f, O = 0.f;
     if (M > -INFINITY) {
 #pragma unroll
-      for (int k = 0; k < kStreams; ++k) {
-        const float w = ex2(cm[k * G + g] - M);
-        L = fmaf(cl[k * G + g], w, L);
-        O = fmaf(co[(k * G + g) * kHeadDim + d], w, O);
+      for (int k = 0; k < kConsumerWarps; ++k) {
+        const float w = ex2(cm[k * G + n] - M);
+        L = fmaf(cl[k * G + n], w, L);
+        O = fmaf(co[(k * G + n) * kHeadDim + d], w, O);
       }
     }
     const float r = L > 0.f ? O / L * vscale : 0.f;
-    p.out[((size_t)s * p.Hq + h * G + g) * kHeadDim + d] = __float2bfloat16_rn(r);
+    p.out[((size_t)s * p.Hq + h * G + n) * kHeadDim + d] = __float2bfloat16_rn(r);
   }
 }
 
-template <int G>
+template <bool kSwz>
 fp8rl_status set_attn_smem(const DeviceState* ds) {
   static bool done[64] = {false};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (ds->device < 64 && done[ds->device]) return FP8RL_OK;
-  fp8rl_status st = cuda_check(cudaFuncSetAttribute(attn_decode_kernel<G>,
+  fp8rl_status st = cuda_check(cudaFuncSetAttribute(attn_decode_kernel<kSwz>,
                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                     (int)kAttnSmem),
                                "cudaFuncSetAttribute(attention)");
@@ -329,12 +493,12 @@ fp8rl_status set_attn_smem(const DeviceState* ds) {
   return st;
 }
 
-template <int G>
+template <bool kSwz>
 fp8rl_status launch_attn(const DeviceState* ds, const CUtensorMap& tk, const CUtensorMap& tv,
                          const AttnParams& p, cudaStream_t stream) {
-  fp8rl_status st = set_attn_smem<G>(ds);
+  fp8rl_status st = set_attn_smem<kSwz>(ds);
   if (st != FP8RL_OK) return st;
-  attn_decode_kernel<G><<<(unsigned)(p.S * p.Hkv), kAttnThreads, kAttnSmem, stream>>>(tk, tv, p);
+  attn_decode_kernel<kSwz><<<(unsigned)(p.S * p.Hkv), kAttnThreads, kAttnSmem, stream>>>(tk, tv, p);
   return cuda_check(cudaGetLastError(), "attn_decode_kernel launch");
 }
 
@@ -381,6 +545,7 @@ extern "C" fp8rl_status fp8rl_decode_attention_fp8kv(
   p.S = num_seqs;
   p.Hq = q_heads;
   p.Hkv = kv_heads;
+  p.G = G;
   p.page = page;
   p.max_pages = max_pages;
   p.num_pages = block_table ? num_pages : num_seqs * max_pages;
@@ -388,22 +553,21 @@ extern "C" fp8rl_status fp8rl_decode_attention_fp8kv(
   p.boxr = block_table ? std::gcd(page, kStageTokens) : kStageTokens;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.status = ds->status;
+  // the 128-byte swizzle wants every box to start on a 1024-byte boundary of
+  // the stage: boxes of a multiple of 8 rows
+  const bool swz = p.boxr % 8 == 0;
+  const CUtensorMapSwizzle mode = swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   // the pool as rows of kv_heads * 128 bytes; a box is one head's 128 bytes
   CUtensorMap tk, tv;
   const uint64_t row_bytes = (uint64_t)kv_heads * kHeadDim;
   if ((st = encode_tiled_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_cache, row_bytes,
-                            (uint64_t)pool_rows, row_bytes, kHeadDim, (uint32_t)p.boxr,
-                            CU_TENSOR_MAP_SWIZZLE_NONE, "K cache")) != FP8RL_OK)
+                            (uint64_t)pool_rows, row_bytes, kHeadDim, (uint32_t)p.boxr, mode,
+                            "K cache")) != FP8RL_OK)
     return st;
   if ((st = encode_tiled_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v_cache, row_bytes,
-                            (uint64_t)pool_rows, row_bytes, kHeadDim, (uint32_t)p.boxr,
-                            CU_TENSOR_MAP_SWIZZLE_NONE, "V cache")) != FP8RL_OK)
+                            (uint64_t)pool_rows, row_bytes, kHeadDim, (uint32_t)p.boxr, mode,
+                            "V cache")) != FP8RL_OK)
     return st;
-  switch (G) {
-    case 1: st = launch_attn<1>(ds, tk, tv, p, stream); break;
-    case 2: st = launch_attn<2>(ds, tk, tv, p, stream); break;
-    case 4: st = launch_attn<4>(ds, tk, tv, p, stream); break;
-    default: st = launch_attn<8>(ds, tk, tv, p, stream); break;
-  }
+  st = swz ? launch_attn<true>(ds, tk, tv, p, stream) : launch_attn<false>(ds, tk, tv, p, stream);
   return st == FP8RL_OK ? ok() : st;
 }

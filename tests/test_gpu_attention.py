@@ -1,10 +1,15 @@
 """GPU parity of the FP8-KV decode attention against the float64 oracle.
 
-Tolerance, from the arithmetic: the kernel dequantizes exactly and works in
-FP32 (scores from 8-term FMA chains plus a 4-level shuffle sum, exp2f within
-2 ulp, running sums over up to len/8 tokens per stream), then rounds to
-BF16.  Per element |out - o| <= 2^-8 |o| + 1e-3 * sum_t p_t |V_t| (BF16
-half-ulp plus FP32 accumulation on the scale of the weighted |V|), and the
+Tolerance, from the arithmetic: the kernel dequantizes exactly (every E4M3
+code is an FP16 value) and scales q per head by a power of two before its
+FP16 conversion (exact in FP16's normal range), so the score products are
+exact and only their FP32 accumulation inside the tensor-core MMA rounds;
+exp2 is within 2 ulp; the probabilities, scaled by 2^15 (so FP16 keeps
+them normal down to p = 2^-29), are rounded to FP16 (relative 2^-11) for the
+weighted sum of V, accumulated in FP32, while the normaliser sums the FP32
+probabilities; the result is rounded to BF16.  Per element
+|out - o| <= 2^-8 |o| + 1e-3 * sum_t p_t |V_t| (BF16 half-ulp, plus the FP16
+probabilities, 2^-11 of the weighted |V|, plus FP32 accumulation), and the
 relative Frobenius error against the BF16-rounded oracle is <= 2e-3."""
 import math
 
@@ -81,6 +86,25 @@ def test_paged_ragged_and_empty():
     _case(2, 8, 2, 96, [96, 95], device(), seed=6, paged=True, page=32)
 
 
+@pytest.mark.parametrize("page", [None, 64, 16, 8, 4, 24])
+def test_many_stages_every_output(page):
+    """64 stages per CTA (4096 tokens) with ragged lengths, contiguous and paged
+    (boxes of 64, 16, 8 rows in the swizzled layout; 4 rows plain; page 24 gives
+    boxes of 8): every output checked, so that a stage read out of turn shows."""
+    dev = device()
+    lens = [4096, 4095, 2049, 64, 65, 1]
+    if page is None:
+        _case(6, 8, 2, 4096, lens, dev, seed=40)
+    else:
+        T = 4096 + (-4096) % page
+        _case(6, 8, 2, T, lens, dev, seed=41 + page, paged=True, page=page)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 2)])
+def test_many_stages_group_sizes(hq, hkv):
+    _case(3, hq, hkv, 3000, [3000, 2999, 1717], device(), seed=50 + hq)
+
+
 def test_quantized_cache_chain():
     """K and V of 4 sequences x 2048 tokens through the KV quantizer (calibrated
     per-head scales), then decode attention of 32 query heads."""
@@ -95,6 +119,7 @@ def test_quantized_cache_chain():
     out = fp8rl.decode_attention_fp8kv(q.to(dev), kq, vq, ks, vs,
                                        torch.tensor(lens, dtype=torch.int32, device=dev))
     torch.cuda.synchronize()
+    fp8rl.device_status(0)
     o64, mag = oracle.decode_attention_fp8kv(q, kq.cpu().numpy(), vq.cpu().numpy(),
                                              ks.cpu().numpy(), vs.cpu().numpy(), lens)
     _check(out, o64, mag, "quantized chain")
@@ -102,7 +127,7 @@ def test_quantized_cache_chain():
 
 def test_long_context_sampled_sequences():
     """64 sequences x 20480 tokens x 8 KV heads (the long-context KV workload),
-    32 query heads; two sequences checked against the oracle."""
+    32 query heads; four sequences checked against the oracle."""
     dev = device()
     S, T, Hkv, Hq = 64, 20480, 8, 32
     k = workloads.kv_tensor(seed=31, device=dev)
@@ -116,7 +141,8 @@ def test_long_context_sampled_sequences():
     lens[5] = 12345
     out = fp8rl.decode_attention_fp8kv(q.to(dev), kq, vq, ks, vs, lens.to(dev))
     torch.cuda.synchronize()
-    for s in (5, 63):
+    fp8rl.device_status(0)
+    for s in (0, 5, 31, 63):
         o64, mag = oracle.decode_attention_fp8kv(q[s:s + 1], kq[s].cpu().numpy()[None],
                                                  vq[s].cpu().numpy()[None], ks.cpu().numpy(),
                                                  vs.cpu().numpy(), [int(lens[s])])
