@@ -8,7 +8,9 @@
 //   o   = sum_t p_t * v_scale[h] * dec(V[t]),      out = BF16(o).
 // Token t of sequence s lives in page block_table[s][t / page], slot t % page.
 //
-// One CTA per (sequence, KV head).  A producer warp TMA-loads the head's
+// A cluster of C CTAs per (sequence, KV head) (C = 1 when the pairs already
+// fill the GPU; up to 8 for small batches), rank r taking a contiguous range
+// of the sequence's 64-token stages.  In each CTA a producer warp TMA-loads the head's
 // 128-byte slice of 64 consecutive tokens of K and of V per stage (16 KB, in
 // the 128-byte swizzled layout when the boxes allow it) into a 6-slot
 // mbarrier ring, with the stage's valid-token mask; its lanes look up the
@@ -31,8 +33,9 @@
 // so that every lane reads whole 16-byte chunks; the score fragment becomes
 // the second product's operand through an in-register transpose (movmatrix).
 // Online softmax in the log2 domain, rescaled once per stage; the three warps
-// are combined through shared memory at the end.  Every mbarrier wait is
-// bounded.
+// are combined through shared memory, then the C ranks of a cluster through
+// distributed shared memory (each rank writes a slice of the output).  Every
+// mbarrier wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -67,9 +70,10 @@ struct AttnShared {
   uint32_t abort_flag;
 };
 constexpr size_t kAttnSmem = 1024 + (size_t)kStages * kStageBytes + sizeof(AttnShared);
-static_assert((size_t)kConsumerWarps * (2 + kHeadDim) * kMaxG * sizeof(float) <=
+static_assert((size_t)(kConsumerWarps + 1) * (2 + kHeadDim) * kMaxG * sizeof(float) <=
                   (size_t)kStages * kStageBytes,
               "the combine buffers must fit in the idle stages");
+constexpr int kMaxCluster = 8;
 
 // 2^x with the hardware approximation (relative error about 2^-22); the
 // attention is compared with a tolerance, not bit for bit.
@@ -129,6 +133,7 @@ struct AttnParams {
   __nv_bfloat16* out;         // [S, Hq, 128]
   int S, Hq, Hkv, G, page, max_pages, num_pages;
   int boxr;                   // rows per TMA box (divides page when paged; 64 if contiguous)
+  int csplit;                 // CTAs per (sequence, KV head): the cluster size
   float sm_scale_log2;        // sm_scale * log2(e)
   uint32_t* status;
 };
@@ -161,7 +166,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
                                              ~static_cast<uintptr_t>(1023));
   AttnShared* sh = reinterpret_cast<AttnShared*>(smem + kStages * kStageBytes);
   volatile uint32_t* abort_flag = &sh->abort_flag;
-  const int s = blockIdx.x / p.Hkv, h = blockIdx.x % p.Hkv;
+  const int C = p.csplit;
+  const uint32_t crank = C > 1 ? cluster_ctarank() : 0u;
+  const int pair = (int)(blockIdx.x / (unsigned)C);
+  const int s = pair / p.Hkv, h = pair % p.Hkv;
   const int G = p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int len = __ldg(p.lens + s);
@@ -170,7 +178,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
     if (tid == 0) atomicOr(p.status, kStatusBadIndex);
     len = cap;
   }
-  const int nst = len > 0 ? (len + kStageTokens - 1) / kStageTokens : 0;
+  const int nst_all = len > 0 ? (len + kStageTokens - 1) / kStageTokens : 0;
+  // this rank's stages: [i0, i0 + nst); j = i - i0 numbers the ring's uses
+  const int i0 = (int)(((int64_t)nst_all * crank) / C);
+  const int nst = (int)(((int64_t)nst_all * (crank + 1)) / C) - i0;
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&sh->full[i]), 1);
@@ -208,11 +219,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
         }
       }
     };
-    if (nst > 0) lookup(0);
+    if (nst > 0) lookup(i0);
     uint32_t issued = 0;
-    for (int i = 0; i < nst; ++i) {
-      const int st = i % kStages;
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+    for (int j = 0; j < nst; ++j) {
+      const int st = j % kStages;
+      const uint32_t ph = (uint32_t)(j / kStages) & 1u;
       bool okw = true;
       if (lane == 0) okw = mbar_wait(smem_u32(&sh->empty[st]), ph ^ 1u, abort_flag, p.status, 31);
       if (!__shfl_sync(0xFFFFFFFFu, okw ? 1 : 0, 0)) break;
@@ -240,7 +251,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
         }
       }
       ++issued;
-      if (i + 1 < nst) lookup(i + 1);   // the page-table loads overlap the next wait
+      if (j + 1 < nst) lookup(i0 + j + 1);   // the page-table loads overlap the next wait
     }
     if (__any_sync(0xFFFFFFFFu, bad_seen) && lane == 0) atomicOr(p.status, kStatusBadIndex);
     if (lane == 0 && issued < (uint32_t)nst) {
@@ -311,11 +322,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
     const uint32_t vofs0 = (uint32_t)((g ^ (kSwz ? 2 * c : 0)) << 4);         // V rows 2c, 2c+8
     const uint32_t vofs1 = (uint32_t)((g ^ (kSwz ? 2 * c + 1 : 0)) << 4);     // V rows 2c+1, 2c+9
 
-    // warp w takes stages w, w+3, ...: a warp-uniform count, so every lane
+    // warp w takes the rank's stages w, w+3, ...: a warp-uniform count, so every lane
     // reaches every full-warp shuffle, MMA and transpose
-    for (int i = warp; i < nst; i += kConsumerWarps) {
-      const int st = i % kStages;
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+    for (int j = warp; j < nst; j += kConsumerWarps) {
+      const int st = j % kStages;
+      const uint32_t ph = (uint32_t)(j / kStages) & 1u;
       bool okw = mbar_wait(smem_u32(&sh->full[st]), ph, abort_flag, p.status, 32);
       okw = __all_sync(0xFFFFFFFFu, okw);
       if (!okw) break;
@@ -460,6 +471,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
   }
   __syncthreads();
   const float vscale = __ldg(p.v_scale + h);
+  // this CTA's state per head: max xm, sum xl, unnormalised xo (C > 1)
+  float* xm = co + kConsumerWarps * G * kHeadDim;        // [G]
+  float* xl = xm + kMaxG;                                // [G]
+  float* xo = xl + kMaxG;                                // [G][128]
   for (int idx = tid; idx < G * kHeadDim; idx += kAttnThreads) {
     const int n = idx / kHeadDim, d = idx - n * kHeadDim;
     float M = -INFINITY;
@@ -474,8 +489,49 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
         O = fmaf(co[(k * G + n) * kHeadDim + d], w, O);
       }
     }
-    const float r = L > 0.f ? O / L * vscale : 0.f;
-    p.out[((size_t)s * p.Hq + h * G + n) * kHeadDim + d] = __float2bfloat16_rn(r);
+    if (C == 1) {
+      const float r = L > 0.f ? O / L * vscale : 0.f;
+      p.out[((size_t)s * p.Hq + h * G + n) * kHeadDim + d] = __float2bfloat16_rn(r);
+    } else {
+      xo[idx] = O;
+      if (d == 0) {
+        xm[n] = M;
+        xl[n] = L;
+      }
+    }
+  }
+  if (C > 1) {
+    // every rank's state is visible after this phase; rank r then writes the
+    // output elements r, r + C*threads, ... reading all ranks' states
+    cluster_arrive();
+    cluster_wait();
+    const uint32_t axm = smem_u32(xm), axl = smem_u32(xl), axo = smem_u32(xo);
+    for (int idx = (int)crank * kAttnThreads + tid; idx < G * kHeadDim; idx += C * kAttnThreads) {
+      const int n = idx / kHeadDim, d = idx - n * kHeadDim;
+      float mr[8];
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        mr[r] = r < C ? ld_cluster_f32(mapa(axm + 4u * n, (uint32_t)r)) : -INFINITY;
+        M = fmaxf(M, mr[r]);
+      }
+      float L = 0.f, O = 0.f;
+      if (M > -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (r < C) {
+            const float w = ex2(mr[r] - M);
+            L = fmaf(ld_cluster_f32(mapa(axl + 4u * n, (uint32_t)r)), w, L);
+            O = fmaf(ld_cluster_f32(mapa(axo + 4u * idx, (uint32_t)r)), w, O);
+          }
+        }
+      }
+      const float res = L > 0.f ? O / L * vscale : 0.f;
+      p.out[((size_t)s * p.Hq + h * G + n) * kHeadDim + d] = __float2bfloat16_rn(res);
+    }
+    // no rank leaves while another may still read its shared memory
+    cluster_arrive();
+    cluster_wait();
   }
 }
 
@@ -493,13 +549,78 @@ fp8rl_status set_attn_smem(const DeviceState* ds) {
   return st;
 }
 
+// Clusters of c attention CTAs that can be resident at once (0 if none).
+template <bool kSwz>
+int attn_active_clusters(const DeviceState* ds, int c) {
+  static int cache[64][kMaxCluster + 1] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  int* slot = ds->device < 64 ? &cache[ds->device][c] : nullptr;
+  if (slot && *slot) return *slot > 0 ? *slot : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)c, 1, 1);
+  cfg.blockDim = dim3(kAttnThreads, 1, 1);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_decode_kernel<kSwz>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  if (slot) *slot = n > 0 ? n : -1;
+  return n;
+}
+
+// Cluster size: double C while all pairs x C CTAs still fit in one resident
+// wave and every rank keeps at least two stages per consumer warp.
+template <bool kSwz>
+int choose_csplit(const DeviceState* ds, int64_t pairs, int64_t nst_cap) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<kSwz>,
+                                                    kAttnThreads, kAttnSmem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    per_sm = 1;
+  }
+  const int64_t slots = (int64_t)ds->sm_count * std::max(per_sm, 1);
+  int c = 1;
+  while (c < kMaxCluster && pairs * c * 2 <= slots && nst_cap / (c * 2) >= 2 * kConsumerWarps)
+    c *= 2;
+  while (c > 1 && attn_active_clusters<kSwz>(ds, c) <= 0) c /= 2;
+  return c;
+}
+
 template <bool kSwz>
 fp8rl_status launch_attn(const DeviceState* ds, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const AttnParams& p, cudaStream_t stream) {
+                         AttnParams p, cudaStream_t stream) {
   fp8rl_status st = set_attn_smem<kSwz>(ds);
   if (st != FP8RL_OK) return st;
-  attn_decode_kernel<kSwz><<<(unsigned)(p.S * p.Hkv), kAttnThreads, kAttnSmem, stream>>>(tk, tv, p);
-  return cuda_check(cudaGetLastError(), "attn_decode_kernel launch");
+  const int64_t pairs = (int64_t)p.S * p.Hkv;
+  const int64_t nst_cap = ((int64_t)p.max_pages * p.page + kStageTokens - 1) / kStageTokens;
+  p.csplit = choose_csplit<kSwz>(ds, pairs, nst_cap);
+  if (p.csplit == 1) {
+    attn_decode_kernel<kSwz><<<(unsigned)pairs, kAttnThreads, kAttnSmem, stream>>>(tk, tv, p);
+    return cuda_check(cudaGetLastError(), "attn_decode_kernel launch");
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(pairs * p.csplit), 1, 1);
+  cfg.blockDim = dim3(kAttnThreads, 1, 1);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.csplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, attn_decode_kernel<kSwz>, tk, tv, p),
+                    "attn_decode_kernel cluster launch");
 }
 
 }  // namespace
@@ -523,7 +644,8 @@ extern "C" fp8rl_status fp8rl_decode_attention_fp8kv(
     return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "q_heads / kv_heads must be 1, 2, 4 or 8");
   if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale))
     return fail(FP8RL_ERR_INVALID_ARG, "sm_scale must be finite and > 0");
-  if ((int64_t)page * max_pages > INT32_MAX || (int64_t)num_seqs * kv_heads > INT32_MAX)
+  if ((int64_t)page * max_pages > INT32_MAX ||
+      (int64_t)num_seqs * kv_heads * kMaxCluster > INT32_MAX)
     return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "sizes too large");
   if (block_table && num_pages < 1)
     return fail(FP8RL_ERR_INVALID_ARG, "a paged cache needs num_pages >= 1");
@@ -553,6 +675,7 @@ extern "C" fp8rl_status fp8rl_decode_attention_fp8kv(
   p.boxr = block_table ? std::gcd(page, kStageTokens) : kStageTokens;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.status = ds->status;
+  p.csplit = 1;   // chosen at launch
   // the 128-byte swizzle wants every box to start on a 1024-byte boundary of
   // the stage: boxes of a multiple of 8 rows
   const bool swz = p.boxr % 8 == 0;

@@ -148,6 +148,13 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t caddr) {
   return v;
 }
 
+// 4-byte load from the shared memory of a CTA of the cluster (address from mapa).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr));
+  return v;
+}
+
 // Named barrier over a subset of the CTA's warps (id 1..15).
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -105,6 +105,14 @@ def test_many_stages_group_sizes(hq, hkv):
     _case(3, hq, hkv, 3000, [3000, 2999, 1717], device(), seed=50 + hq)
 
 
+@pytest.mark.parametrize("paged", [False, True])
+def test_cluster_split_short_and_long(paged):
+    """Few (sequence, head) pairs over long contexts run as clusters of up to 8
+    CTAs, each over a range of stages; the short sequence leaves most ranks
+    with no stage at all."""
+    _case(2, 8, 2, 8192, [8192, 100], device(), seed=60 + int(paged), paged=paged, page=32)
+
+
 def test_quantized_cache_chain():
     """K and V of 4 sequences x 2048 tokens through the KV quantizer (calibrated
     per-head scales), then decode attention of 32 query heads."""
