@@ -12,7 +12,8 @@ Cases (device footprint in parentheses):
   grouped         grouped W8A8 GEMM, Qwen3-30B-A3B gate_up, 128 experts (0.5 GB)
   kv              KV calibrate + quantize, 8 x 20480 tokens x 8 x 128 (0.5 GB)
   tis             TIS weights over 64 x 20480 tokens (0.02 GB)
-  attention       FP8-KV decode attention, 8 seqs x 20480 tokens, 32 q / 8 KV heads (0.7 GB)
+  attention       FP8-KV decode attention, 64 seqs x 4096 tokens, 32 q / 8 KV heads (0.6 GB;
+                  one CTA per sequence and KV head, as at 64 x 20480)
   glue_gather     MoE gather + quantize: 4096 tokens x 2048 -> 32768 routed rows (0.1 GB)
   glue_silu       MoE SiLU(gate)*up + quantize: 32768 x 1536 -> 32768 x 768 (0.13 GB)
 """
@@ -72,12 +73,12 @@ def main(argv=None):
         lt, lr = wl.tis_logprobs(64 * 20480, seed=5, device=dev, kind="student_t")
         run = lambda: fp8rl.tis_weights(lt, lr)  # noqa: E731
     elif c == "attention":
-        k = wl.kv_tensor(seed=6, device=dev, seqs=8)
+        k = wl.kv_tensor(seed=6, device=dev, seqs=64, tokens=4096)
         kq, ks = fp8rl.quantize_kv_fp8(k, fp8rl.FP8RL_KV_CALIBRATE)
         vq, vs = fp8rl.quantize_kv_fp8(k, fp8rl.FP8RL_KV_CALIBRATE)
         del k
-        qh = torch.randn(8, 32, 128, device=dev).to(torch.bfloat16)
-        lens = torch.full((8,), 20480, dtype=torch.int32, device=dev)
+        qh = torch.randn(64, 32, 128, device=dev).to(torch.bfloat16)
+        lens = torch.full((64,), 4096, dtype=torch.int32, device=dev)
         run = lambda: fp8rl.decode_attention_fp8kv(qh, kq, vq, ks, vs, lens)  # noqa: E731
     elif c == "glue_gather":
         _, tok, _ = wl.moe_routing(seed=0)
