@@ -109,7 +109,6 @@ class ClockSampler:
 # it is reported only while the kernel's sources hash to the captured value.
 WQ_SOURCES = ["fp8_precision_rollout_gb300/csrc/quant.cu",
               "fp8_precision_rollout_gb300/csrc/fp_exact.cuh",
-              "fp8_precision_rollout_gb300/csrc/sm100_ptx.cuh",
               "fp8_precision_rollout_gb300/csrc/internal.h"]
 WQ_PROFILE = "profiles/wquant_kernel_qwen3_8b_layer0.md"
 

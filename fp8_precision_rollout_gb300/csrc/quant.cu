@@ -20,7 +20,6 @@
 
 #include "fp_exact.cuh"
 #include "internal.h"
-#include "sm100_ptx.cuh"
 
 namespace fp8rl {
 namespace {
@@ -119,46 +118,35 @@ __device__ __forceinline__ float warp_max(float v, int width) {
 
 // -------------------------------------------------- 128x128 weight blocks --
 //
-// Persistent, TMA-fed: each CTA walks blocks blockIdx.x, +gridDim.x, ... of
-// all tensors of the launch.  A producer warp streams each 128x128 BF16 block
-// (32 KB) into a 2-stage shared-memory ring with one 2-D TMA load; eight
-// consumer warps copy the block to registers, release the stage, reduce the
-// block max (warp shuffles + a named barrier), and write the codes with 8-byte
-// stores.  Loads of the next blocks stay in flight across each block's
-// max -> quantize dependency; three CTAs per SM keep ~192 KB in flight.  Edge
-// blocks are zero-filled by TMA outside the tensor, which leaves the max of
-// the valid elements unchanged; stores are masked to the valid region.
+// Persistent: each CTA (256 threads, 2 per SM) walks blocks blockIdx.x,
+// +gridDim.x, ... of all tensors of the launch.  Thread t holds rows t/16 +
+// 16j (j < 8) and columns (t%16)*8 .. +8 of a block in registers, loaded with
+// 16-byte non-allocating loads, so the block max and the codes need a single
+// HBM read.  The next block's loads are issued before the current block is
+// quantized: two blocks per CTA are in flight.  The block max is a bf16x2
+// max over bit patterns, warp shuffles and one CTA barrier; codes go out as
+// 8-byte stores.  Edge blocks load zeros outside the tensor (the max of the
+// valid elements is unchanged) and mask their stores.  A CTA visits blocks in
+// increasing order, so its tensor index only moves forward.
 
 constexpr int kWQMaxDescs = 160;
-constexpr int kWQStages = 2;
-constexpr int kWQBlockBytes = 128 * 128 * 2;
-constexpr int kWQConsumerThreads = 256;
-constexpr int kWQThreads = kWQConsumerThreads + 32;
+constexpr int kWQThreads = 256;
 
 struct WQDesc {
+  const uint16_t* w;
   uint8_t* q;
   float* scales;
-  int64_t ldq;
+  int64_t ldw, ldq;
   int32_t n, k, kb, pad;
 };
 
 struct WQParams {
-  CUtensorMap map[kWQMaxDescs];     // BF16 [n, k], row pitch ldw*2, box 128 x 128, no swizzle
   WQDesc d[kWQMaxDescs];
   int32_t start[kWQMaxDescs + 1];   // first block id of each tensor; start[count] = total
   int32_t count;
   int32_t total;
   uint32_t* status;
 };
-
-struct WQShared {
-  uint64_t full[kWQStages];
-  uint64_t empty[kWQStages];
-  float red[2][8];
-  uint32_t abort_flag;
-};
-
-constexpr size_t kWQSmem = 1024 + (size_t)kWQStages * kWQBlockBytes + sizeof(WQShared);
 
 __device__ __forceinline__ int wq_find(const WQParams& p, int b) {
   int lo = 0, hi = p.count - 1;
@@ -169,99 +157,85 @@ __device__ __forceinline__ int wq_find(const WQParams& p, int b) {
   return lo;
 }
 
-__global__ void __launch_bounds__(kWQThreads, 3) wquant_kernel(const __grid_constant__ WQParams p) {
-  using namespace ptx;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  WQShared* sh = reinterpret_cast<WQShared*>(smem + kWQStages * kWQBlockBytes);
-  volatile uint32_t* abort_flag = &sh->abort_flag;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    for (int s = 0; s < kWQStages; ++s) {
-      mbar_init(smem_u32(&sh->full[s]), 1);
-      mbar_init(smem_u32(&sh->empty[s]), kWQConsumerThreads / 32);
-    }
-    sh->abort_flag = 0;
-    mbar_fence_init();
-  }
-  __syncthreads();
+struct WQBlock {
+  int t, bi, bj;
+};
 
-  if (warp == kWQConsumerThreads / 32) {
-    // ------------------------------------------------------------ producer --
-    if (lane == 0) {
-      uint32_t i = 0;
-      for (int b = blockIdx.x; b < p.total; b += gridDim.x, ++i) {
-        const int t = wq_find(p, b);
-        const WQDesc& d = p.d[t];
-        const int local = b - p.start[t];
-        const int bi = local / d.kb, bj = local - (local / d.kb) * d.kb;
-        const int s = i % kWQStages;
-        const uint32_t ph = (i / kWQStages) & 1u;
-        if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.status, 21)) {
-          // let the loads already issued land before the CTA exits
-          const uint32_t n = i < (uint32_t)kWQStages ? i : (uint32_t)kWQStages;
-          for (uint32_t j = 1; j <= n; ++j)
-            mbar_drain(smem_u32(&sh->full[(i - j) % kWQStages]), ((i - j) / kWQStages) & 1u,
-                       p.status, 22);
-          break;
-        }
-        const uint32_t fb = smem_u32(&sh->full[s]);
-        mbar_expect_tx(fb, kWQBlockBytes);
-        tma_load_2d(smem_u32(smem + s * kWQBlockBytes), &p.map[t], fb, bj * 128, bi * 128);
+// Block b of the launch; blocks are visited in increasing order by a CTA, so
+// the tensor index only moves forward from the previous block's (t).
+__device__ __forceinline__ WQBlock wq_block(const WQParams& p, int b, int t) {
+  WQBlock x;
+  while (t + 1 < p.count && p.start[t + 1] <= b) ++t;
+  x.t = t;
+  const int local = b - p.start[x.t];
+  const int kb = p.d[x.t].kb;
+  x.bi = local / kb;
+  x.bj = local - x.bi * kb;
+  return x;
+}
+
+// thread tid holds rows bi*128 + tid/16 + 16j (j < 8), columns bj*128 + (tid%16)*8 .. +8
+__device__ __forceinline__ void wq_load(const WQParams& p, const WQBlock& x, int tid, uint4 (&v)[8]) {
+  const WQDesc& d = p.d[x.t];
+  const int col = x.bj * 128 + (tid & 15) * 8;
+  const int r0 = x.bi * 128 + (tid >> 4);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = r0 + 16 * j;
+    v[j] = (r < d.n && col < d.k) ? ld_stream(d.w + (int64_t)r * d.ldw + col) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+__global__ void __launch_bounds__(kWQThreads) wquant_kernel(const __grid_constant__ WQParams p) {
+  __shared__ float red[2][8];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint4 cur[8], nxt[8];
+  int b = blockIdx.x;
+  WQBlock xc = {0, 0, 0}, xn = {0, 0, 0};
+  if (b < p.total) {
+    xc = wq_block(p, b, wq_find(p, b));
+    wq_load(p, xc, tid, cur);
+  }
+  xn = xc;
+  for (uint32_t i = 0; b < p.total; b += gridDim.x, ++i) {
+    const int bn = b + gridDim.x;
+    if (bn < p.total) {
+      xn = wq_block(p, bn, xn.t);
+      wq_load(p, xn, tid, nxt);
+    }
+    const WQDesc& d = p.d[xc.t];
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m2 = absmax8(m2, cur[j]);
+    float amax = warp_max(bf16x2_maxf(m2), 32);
+    if (lane == 0) red[i & 1][warp] = amax;
+    __syncthreads();
+    amax = red[i & 1][0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[i & 1][w]);
+    const float sc = fx::fdiv(amax, 448.0f);
+    if (tid == 0) d.scales[(int64_t)xc.bi * d.kb + xc.bj] = sc;
+    const ScaleDiv sd = make_scale_div(sc);
+    const int col = xc.bj * 128 + (tid & 15) * 8;
+    const int row0 = xc.bi * 128 + (tid >> 4);
+    const bool full = (xc.bi * 128 + 128 <= d.n) && (xc.bj * 128 + 128 <= d.k);
+    if (full && sd.mode == 1) {
+      uint8_t* qp = d.q + (int64_t)row0 * d.ldq + col;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint2*>(qp + (int64_t)(16 * j) * d.ldq) =
+            quant8_fast<false>(cur[j], sd.s, sd.y);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = row0 + 16 * j;
+        if (r < d.n && col < d.k)
+          *reinterpret_cast<uint2*>(d.q + (int64_t)r * d.ldq + col) = quant8<false>(cur[j], sd);
       }
     }
-    __syncwarp();
-  } else {
-    // ----------------------------------------------------------- consumers --
-    uint32_t i = 0;
-    for (int b = blockIdx.x; b < p.total; b += gridDim.x, ++i) {
-      const int t = wq_find(p, b);
-      const WQDesc& d = p.d[t];
-      const int local = b - p.start[t];
-      const int bi = local / d.kb, bj = local - (local / d.kb) * d.kb;
-      const int s = i % kWQStages;
-      const uint32_t ph = (i / kWQStages) & 1u;
-      bool okw = mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.status, 23);
-      okw = __all_sync(0xFFFFFFFFu, okw);
-      if (!okw) break;
-      // chunk c = tid + 256 j of the block: row c / 16, columns (c % 16) * 8 .. + 8
-      const uint4* stage = reinterpret_cast<const uint4*>(smem + s * kWQBlockBytes);
-      uint4 v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = stage[tid + kWQConsumerThreads * j];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh->empty[s]));
-      uint32_t m2 = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) m2 = absmax8(m2, v[j]);
-      float amax = warp_max(bf16x2_maxf(m2), 32);
-      if (lane == 0) sh->red[i & 1][warp] = amax;
-      named_bar(1, kWQConsumerThreads);
-      amax = sh->red[i & 1][0];
-#pragma unroll
-      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, sh->red[i & 1][w]);
-      const float sc = fx::fdiv(amax, 448.0f);
-      if (tid == 0) d.scales[(int64_t)bi * d.kb + bj] = sc;
-      const ScaleDiv sd = make_scale_div(sc);
-      const int col = bj * 128 + (tid & 15) * 8;
-      const int row0 = bi * 128 + (tid >> 4);
-      const bool full = (bi * 128 + 128 <= d.n) && (bj * 128 + 128 <= d.k);
-      if (full && sd.mode == 1) {
-        uint8_t* qp = d.q + (int64_t)row0 * d.ldq + col;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint2*>(qp + (int64_t)(16 * j) * d.ldq) =
-              quant8_fast<false>(v[j], sd.s, sd.y);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = row0 + 16 * j;
-          if (r < d.n && col < d.k)
-            *reinterpret_cast<uint2*>(d.q + (int64_t)r * d.ldq + col) = quant8<false>(v[j], sd);
-        }
-      }
-    }
+    for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+    xc = xn;
   }
 }
 
@@ -529,15 +503,8 @@ extern "C" fp8rl_status fp8rl_quantize_weights_blockwise_multi(const fp8rl_wdesc
   if (st != FP8RL_OK) return st;
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
-  static bool attr_done[64] = {false};
-  if (ds->device < 64 && !attr_done[ds->device]) {
-    st = cuda_check(cudaFuncSetAttribute(wquant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kWQSmem),
-                    "cudaFuncSetAttribute(wquant)");
-    if (st != FP8RL_OK) return st;
-    attr_done[ds->device] = true;
-  }
-  static WQParams p;   // ~25 KB of kernel parameters, filled per launch under the lock
+  static const int per_sm = resident_ctas_per_sm(wquant_kernel, kWQThreads);
+  static WQParams p;   // ~10 KB of kernel parameters, filled per launch under the lock
   for (int base = 0; base < count; base += kWQMaxDescs) {
     const int c = std::min(kWQMaxDescs, count - base);
     std::memset(&p, 0, sizeof(p));
@@ -548,10 +515,8 @@ extern "C" fp8rl_status fp8rl_quantize_weights_blockwise_multi(const fp8rl_wdesc
       const fp8rl_wdesc& d = descs[base + i];
       const int64_t kb = (d.k + 127) / 128;
       p.start[i] = (int32_t)total;
-      st = encode_tiled_2d(&p.map[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.w, (uint64_t)d.k,
-                           (uint64_t)d.n, (uint64_t)d.ldw * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE,
-                           "weight");
-      if (st != FP8RL_OK) return st;
+      p.d[i].w = reinterpret_cast<const uint16_t*>(d.w);
+      p.d[i].ldw = d.ldw;
       p.d[i].q = d.q;
       p.d[i].scales = d.scales;
       p.d[i].ldq = d.ldq;
@@ -564,8 +529,8 @@ extern "C" fp8rl_status fp8rl_quantize_weights_blockwise_multi(const fp8rl_wdesc
     }
     p.start[c] = (int32_t)total;
     p.total = (int32_t)total;
-    const int grid = (int)std::min<int64_t>(total, (int64_t)ds->sm_count * 3);
-    wquant_kernel<<<grid, kWQThreads, kWQSmem, stream>>>(p);
+    const int grid = (int)std::min<int64_t>(total, (int64_t)ds->sm_count * per_sm);
+    wquant_kernel<<<grid, kWQThreads, 0, stream>>>(p);
     st = cuda_check(cudaGetLastError(), "wquant_kernel launch");
     if (st != FP8RL_OK) return st;
   }
