@@ -31,6 +31,10 @@ struct DeviceState {
 // that it is an sm_103 part.  On failure returns a status (message set).
 fp8rl_status device_state(DeviceState** out);
 
+// Builds the per-device lookup tables of the MoE glue (quant.cu); called once
+// per device when its state is created, synchronously.
+fp8rl_status init_glue_tables();
+
 // Device status word bits.
 enum : uint32_t {
   kStatusTimeout = 1u << 0,   // a pipelined kernel gave up on an mbarrier wait

@@ -345,16 +345,30 @@ __device__ __forceinline__ uint32_t bf16_rne_bits(float f) {
   return b >> 16;
 }
 
+// silu(g) = fl32(g / fl32(1 + E(-g))) for every BF16 gate g, indexed by its
+// 16 bits.  The glue's activation depends on the gate alone, so it is formed
+// once per device (init_glue_tables, at the library's first use of the
+// device) with exactly this arithmetic, and the kernel looks it up.
+__device__ float g_silu_tab[65536];
+
+__global__ void silu_table_kernel() {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < 65536) {
+    const float g = __uint_as_float((uint32_t)i << 16);
+    const float den = fx::fadd(1.0f, glue_exp32(-g));
+    g_silu_tab[i] = fx::fdiv(g, den);
+  }
+}
+
 // Two BF16 lanes (packed in a 32-bit word) of gate and up -> the packed BF16
 // pair silu(g) * u.
 __device__ __forceinline__ uint32_t silu_mul2(uint32_t g2, uint32_t u2) {
   uint32_t out = 0;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const float g = __uint_as_float((h ? (g2 >> 16) : (g2 & 0xFFFFu)) << 16);
+    const uint32_t gb = h ? (g2 >> 16) : (g2 & 0xFFFFu);
     const float u = __uint_as_float((h ? (u2 >> 16) : (u2 & 0xFFFFu)) << 16);
-    const float den = fx::fadd(1.0f, glue_exp32(-g));
-    const float y = fx::fmul(fx::fdiv(g, den), u);
+    const float y = fx::fmul(__ldg(&g_silu_tab[gb]), u);
     out |= bf16_rne_bits(y) << (16 * h);
   }
   return out;
@@ -590,6 +604,15 @@ extern "C" fp8rl_status fp8rl_quantize_act_gather(const void* a, int64_t m_src, 
   st = cuda_check(cudaGetLastError(), "aquant_kernel (gather) launch");
   return st == FP8RL_OK ? ok() : st;
 }
+
+namespace fp8rl {
+fp8rl_status init_glue_tables() {
+  silu_table_kernel<<<65536 / 256, 256>>>();
+  fp8rl_status st = cuda_check(cudaGetLastError(), "silu_table_kernel launch");
+  if (st != FP8RL_OK) return st;
+  return cuda_check(cudaDeviceSynchronize(), "building the SiLU table");
+}
+}  // namespace fp8rl
 
 extern "C" fp8rl_status fp8rl_silu_mul_quantize(const void* h, int64_t m, int64_t inter,
                                                 int64_t ldh, uint8_t* q, float* scales,

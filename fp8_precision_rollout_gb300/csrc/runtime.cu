@@ -58,6 +58,11 @@ fp8rl_status device_state(DeviceState** out) {
     if (e != cudaSuccess) return cuda_check(e, "cudaMalloc(workspace)");
     e = cudaMemset(ws, 0, kWorkspaceBytes);
     if (e != cudaSuccess) return cuda_check(e, "cudaMemset(workspace)");
+    const fp8rl_status ts = init_glue_tables();
+    if (ts != FP8RL_OK) {
+      cudaFree(ws);
+      return ts;
+    }
     st.sm_count = prop.multiProcessorCount;
     st.cc_major = prop.major;
     st.cc_minor = prop.minor;

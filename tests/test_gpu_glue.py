@@ -118,3 +118,17 @@ def test_silu_row_stride_and_special_values():
     h = torch.from_numpy(np.concatenate([g, u], axis=1)).to(torch.bfloat16)
     _silu_case(h, dev)
     _silu_case(h, dev, ld_pad=16)
+
+
+def test_silu_every_bf16_gate():
+    """All 65536 BF16 gate bit patterns (NaN, infinities, subnormals, both
+    zeros) against the oracle, each with three up values: the activation is a
+    function of the gate alone, so this covers every value it can take."""
+    dev = device()
+    gates = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    g = gates.view(512, 128)
+    rng = np.random.default_rng(13)
+    for up in (torch.ones(512, 128), torch.from_numpy(rng.normal(0, 3, (512, 128)).astype(np.float32)),
+               torch.full((512, 128), -1e-3)):
+        h = torch.cat([g, up.to(torch.bfloat16)], dim=1)
+        _silu_case(h, dev)
