@@ -107,7 +107,8 @@ class ClockSampler:
 # The re-quantization kernel's DRAM traffic per element comes from a committed
 # ncu capture (profiles/wquant_kernel_qwen3_8b_layer0.md, line "bench-traffic:");
 # it is reported only while the kernel's sources hash to the captured value.
-WQ_SOURCES = ["fp8_precision_rollout_gb300/csrc/quant.cu",
+WQ_SOURCES = ["fp8_precision_rollout_gb300/csrc/wquant.cu",
+              "fp8_precision_rollout_gb300/csrc/quant_common.cuh",
               "fp8_precision_rollout_gb300/csrc/fp_exact.cuh",
               "fp8_precision_rollout_gb300/csrc/internal.h"]
 WQ_PROFILE = "profiles/wquant_kernel_qwen3_8b_layer0.md"
