@@ -112,6 +112,9 @@ WQ_SOURCES = ["fp8_precision_rollout_gb300/csrc/wquant.cu",
               "fp8_precision_rollout_gb300/csrc/fp_exact.cuh",
               "fp8_precision_rollout_gb300/csrc/internal.h"]
 WQ_PROFILE = "profiles/wquant_kernel_qwen3_8b_layer0.md"
+# The workload the headline metric is quoted on (both arms).
+WORKLOAD = ("qwen3-8b per-step weight re-quantization (36x4 linears, 6.95 G elements, "
+            "128x128 E4M3 blocks)")
 
 
 def sources_sha256(files=WQ_SOURCES) -> str:
@@ -391,7 +394,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16->e4m3", "data": "synthetic",
-            "config": {"workload": "qwen3-8b per-step weight re-quantization, 128x128 E4M3 blocks",
+            "config": {"workload": WORKLOAD,
                        "sample": "layer-0 gate_up [24576, 4096] per step"},
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.threads(),
                              "kind": "oracle",
@@ -492,9 +495,9 @@ def run_ours(args):
                 "ms_per_step": total_ms / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3; e4m3xe4m3->f32->bf16",
                 "data": "synthetic",
-                "config": {"workload": "qwen3-8b per-step weight re-quantization (36x4 linears, "
-                                       "6.95 G elements, 128x128 E4M3 blocks) within a full "
-                                       "hot-path step",
+                "config": {"workload": WORKLOAD,
+                           "step": "timed inside the full hot-path step (GEMMs, MoE chain, KV, "
+                                   "decode attention, TIS, MIS)",
                            "parallelism": "replicas" if world > 1 else "single",
                            "l2": "inputs larger than L2: each step streams ~35 GB"},
                 "roofline": dom, "rows": rows, "gpu_launches": launches,
