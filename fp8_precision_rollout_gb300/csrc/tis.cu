@@ -6,10 +6,12 @@
 // experiments; the same section also states the two-sided range [1/C, C]).
 // Here d = fl32(logp_train - logp_rollout), e = RN32(e^d) exactly (see
 // fp_exact.cuh), w = min(e, c_hi), then max(w, c_lo) when c_lo > 0, NaN kept,
-// and w = 0 for masked-out tokens.  Elementwise: 16-byte loads, 8 tokens per
-// thread per round with all loads issued first, grid-stride; each lane holds
+// and w = 0 for masked-out tokens.  Elementwise: 16-byte loads, 8 to 16 tokens
+// per thread per round with all loads issued first, sized so that one resident
+// wave covers the input (grid-stride beyond that); each lane holds
 // one entry of the 2^(j/32) table in registers and lanes fetch theirs with a
 // warp shuffle.
+#include <algorithm>
 #include <cmath>
 
 #include "fp_exact.cuh"
@@ -62,10 +64,12 @@ __device__ __forceinline__ void tis_store4(float4 r, int64_t i, const uint8_t* _
   reinterpret_cast<float4*>(w)[i] = r;
 }
 
-// A warp task is 64 consecutive 4-token vectors: lane l takes vectors l and
-// l + 32, both loaded before either is computed (two DRAM round trips in
-// flight per thread).  Warp-uniform trip count so every lane reaches the
-// shuffles.
+// A warp task is 32*V consecutive 4-token vectors: lane l takes vectors
+// l + 32u (u < V), all loaded before any is computed.  The host picks the
+// smallest V in [2, 4] for which one resident wave of warps covers the whole
+// input, so no token waits for a second round of load latency.  Warp-uniform
+// trip count so every lane reaches the shuffles.
+template <int V>
 __global__ void __launch_bounds__(256) tis_kernel(const float* __restrict__ lt,
                                                   const float* __restrict__ lr,
                                                   const uint8_t* __restrict__ mask, int64_t n,
@@ -79,18 +83,21 @@ __global__ void __launch_bounds__(256) tis_kernel(const float* __restrict__ lt,
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const float4* lt4 = reinterpret_cast<const float4*>(lt);
   const float4* lr4 = reinterpret_cast<const float4*>(lr);
-  for (int64_t v0 = gw * 64; v0 < n4; v0 += nwarps * 64) {
-    const int64_t i = v0 + lane, i2 = i + 32;
-    const bool in = i < n4, in2 = i2 < n4;
+  for (int64_t v0 = gw * (32 * V); v0 < n4; v0 += nwarps * (32 * V)) {
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 a = in ? __ldg(lt4 + i) : z;
-    const float4 b = in ? __ldg(lr4 + i) : z;
-    const float4 a2 = in2 ? __ldg(lt4 + i2) : z;
-    const float4 b2 = in2 ? __ldg(lr4 + i2) : z;
-    const float4 r = tis_four(a, b, c_hi, c_lo, th_lane, tl_lane, T);
-    if (in) tis_store4(r, i, mask, w);
-    const float4 r2 = tis_four(a2, b2, c_hi, c_lo, th_lane, tl_lane, T);
-    if (in2) tis_store4(r2, i2, mask, w);
+    float4 a[V], b[V];
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const int64_t i = v0 + lane + 32 * u;
+      a[u] = i < n4 ? __ldg(lt4 + i) : z;
+      b[u] = i < n4 ? __ldg(lr4 + i) : z;
+    }
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const int64_t i = v0 + lane + 32 * u;
+      const float4 r = tis_four(a[u], b[u], c_hi, c_lo, th_lane, tl_lane, T);
+      if (i < n4) tis_store4(r, i, mask, w);
+    }
   }
   // ragged tail (n % 4 tokens): the first warp of block 0
   const int64_t tail = n - (n4 << 2);
@@ -203,7 +210,7 @@ __device__ __forceinline__ uint32_t valid_bits(const uint8_t* __restrict__ mask,
 
 // Same traversal as tis_kernel; the statistics are reduced per CTA and added
 // to stats[5] (cleared beforehand) with one FP64 atomic each.
-template <int kMode, bool kW>
+template <int kMode, bool kW, int V>
 __global__ void __launch_bounds__(256) is_stats_kernel(const float* __restrict__ lt,
                                                        const float* __restrict__ lr,
                                                        const uint8_t* __restrict__ mask, int64_t n,
@@ -220,22 +227,24 @@ __global__ void __launch_bounds__(256) is_stats_kernel(const float* __restrict__
   const float4* lt4 = reinterpret_cast<const float4*>(lt);
   const float4* lr4 = reinterpret_cast<const float4*>(lr);
   IsAcc acc;
-  for (int64_t v0 = gw * 64; v0 < n4; v0 += nwarps * 64) {
-    const int64_t i = v0 + lane, i2 = i + 32;
-    const bool in = i < n4, in2 = i2 < n4;
+  for (int64_t v0 = gw * (32 * V); v0 < n4; v0 += nwarps * (32 * V)) {
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 a = in ? __ldg(lt4 + i) : z;
-    const float4 b = in ? __ldg(lr4 + i) : z;
-    const float4 a2 = in2 ? __ldg(lt4 + i2) : z;
-    const float4 b2 = in2 ? __ldg(lr4 + i2) : z;
-    const uint32_t m1 = valid_bits(mask, i, in), m2 = valid_bits(mask, i2, in2);
-    const float4 r = is_four<kMode>(a, b, m1, c_hi, c_lo, th_lane, tl_lane, T, acc);
-    const float4 r2 = is_four<kMode>(a2, b2, m2, c_hi, c_lo, th_lane, tl_lane, T, acc);
-    acc.fold();
-    if (kW) {
-      if (in) reinterpret_cast<float4*>(w)[i] = r;
-      if (in2) reinterpret_cast<float4*>(w)[i2] = r2;
+    float4 a[V], b[V];
+    uint32_t mb[V];
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const int64_t i = v0 + lane + 32 * u;
+      a[u] = i < n4 ? __ldg(lt4 + i) : z;
+      b[u] = i < n4 ? __ldg(lr4 + i) : z;
+      mb[u] = valid_bits(mask, i, i < n4);
     }
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const int64_t i = v0 + lane + 32 * u;
+      const float4 r = is_four<kMode>(a[u], b[u], mb[u], c_hi, c_lo, th_lane, tl_lane, T, acc);
+      if (kW && i < n4) reinterpret_cast<float4*>(w)[i] = r;
+    }
+    acc.fold();
   }
   // ragged tail (n % 4 tokens): the first warp of block 0
   const int64_t tail = n - (n4 << 2);
@@ -270,6 +279,55 @@ __global__ void __launch_bounds__(256) is_stats_kernel(const float* __restrict__
   }
 }
 
+// Vectors per lane V in [2, 4] and grid: the smallest V for which one
+// resident wave of warps (per_sm[V - 2] CTAs of 8 warps per SM) takes every
+// 4-token vector in a single task.  Inputs too large for that run V = 2 in a
+// grid-stride loop (the fewest registers, the most resident warps).
+struct WaveFit {
+  int v;
+  int64_t ctas;
+};
+WaveFit fit_wave(int64_t n, int sms, const int per_sm[3]) {
+  const int64_t n4 = std::max<int64_t>(n >> 2, 1);
+  for (int v = 2; v <= 4; ++v) {
+    const int64_t tasks = (n4 + 32 * v - 1) / (32 * v);
+    const int64_t ctas = (tasks + 7) / 8;
+    const int64_t cap = (int64_t)sms * std::max(per_sm[v - 2], 1);
+    if (ctas <= cap) return {v, ctas};
+  }
+  return {2, (int64_t)sms * std::max(per_sm[0], 1)};
+}
+
+template <int kMode, bool kW>
+void launch_is_stats_v(int sms, cudaStream_t stream, const float* lt, const float* lr,
+                       const uint8_t* mask, int64_t n, float c_hi, float c_lo, float* w,
+                       double* stats, const fx::Exp2Table& T) {
+  static const int per_sm[3] = {resident_ctas_per_sm(is_stats_kernel<kMode, kW, 2>, 256),
+                                resident_ctas_per_sm(is_stats_kernel<kMode, kW, 3>, 256),
+                                resident_ctas_per_sm(is_stats_kernel<kMode, kW, 4>, 256)};
+  const WaveFit f = fit_wave(n, sms, per_sm);
+  const int v = f.v;
+  const unsigned grid = (unsigned)f.ctas;
+  if (v == 2)
+    is_stats_kernel<kMode, kW, 2><<<grid, 256, 0, stream>>>(lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+  else if (v == 3)
+    is_stats_kernel<kMode, kW, 3><<<grid, 256, 0, stream>>>(lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+  else
+    is_stats_kernel<kMode, kW, 4><<<grid, 256, 0, stream>>>(lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+}
+
+void launch_is_stats(int32_t mode, bool with_w, int sms, cudaStream_t stream, const float* lt,
+                     const float* lr, const uint8_t* mask, int64_t n, float c_hi, float c_lo,
+                     float* w, double* stats, const fx::Exp2Table& T) {
+  if (mode == FP8RL_IS_TRUNCATE) {
+    if (with_w) launch_is_stats_v<0, true>(sms, stream, lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+    else launch_is_stats_v<0, false>(sms, stream, lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+  } else {
+    if (with_w) launch_is_stats_v<1, true>(sms, stream, lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+    else launch_is_stats_v<1, false>(sms, stream, lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+  }
+}
+
 }  // namespace
 }  // namespace fp8rl
 
@@ -290,12 +348,17 @@ extern "C" fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* 
   if (st != FP8RL_OK) return st;
   if (n == 0) return ok();
   static const fx::Exp2Table T = fx::make_exp_tables();
-  const int64_t threads_needed = std::max<int64_t>((n + 7) / 8, 1);   // 8 tokens per thread
-  int64_t ctas = (threads_needed + 255) / 256;
-  static const int per_sm = resident_ctas_per_sm(tis_kernel, 256);
-  ctas = std::min<int64_t>(ctas, (int64_t)ds->sm_count * per_sm);
-  tis_kernel<<<(unsigned)ctas, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi, c_lo, w,
-                                                 T);
+  static const int per_sm[3] = {resident_ctas_per_sm(tis_kernel<2>, 256),
+                                resident_ctas_per_sm(tis_kernel<3>, 256),
+                                resident_ctas_per_sm(tis_kernel<4>, 256)};
+  const WaveFit f = fit_wave(n, ds->sm_count, per_sm);
+  const unsigned grid = (unsigned)f.ctas;
+  if (f.v == 2)
+    tis_kernel<2><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi, c_lo, w, T);
+  else if (f.v == 3)
+    tis_kernel<3><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi, c_lo, w, T);
+  else
+    tis_kernel<4><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi, c_lo, w, T);
   st = cuda_check(cudaGetLastError(), "tis_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }
@@ -321,26 +384,8 @@ extern "C" fp8rl_status fp8rl_is_weights_stats(const float* logp_train, const fl
   st = cuda_check(cudaMemsetAsync(stats, 0, 5 * sizeof(double), stream), "cudaMemsetAsync(stats)");
   if (st != FP8RL_OK || n == 0) return st == FP8RL_OK ? ok() : st;
   static const fx::Exp2Table T = fx::make_exp_tables();
-  const int64_t threads_needed = std::max<int64_t>((n + 7) / 8, 1);
-  int64_t ctas = (threads_needed + 255) / 256;
-  static const int per_sm = resident_ctas_per_sm(is_stats_kernel<0, true>, 256);
-  ctas = std::min<int64_t>(ctas, (int64_t)ds->sm_count * per_sm);
-  const unsigned grid = (unsigned)ctas;
-  if (mode == FP8RL_IS_TRUNCATE) {
-    if (w)
-      is_stats_kernel<0, true><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi,
-                                                        c_lo, w, stats, T);
-    else
-      is_stats_kernel<0, false><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi,
-                                                         c_lo, w, stats, T);
-  } else {
-    if (w)
-      is_stats_kernel<1, true><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi,
-                                                        c_lo, w, stats, T);
-    else
-      is_stats_kernel<1, false><<<grid, 256, 0, stream>>>(logp_train, logp_rollout, mask, n, c_hi,
-                                                         c_lo, w, stats, T);
-  }
+  launch_is_stats(mode, w != nullptr, ds->sm_count, stream, logp_train, logp_rollout, mask, n,
+                  c_hi, c_lo, w, stats, T);
   st = cuda_check(cudaGetLastError(), "is_stats_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }
