@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     gemm_w8a8_blockwise,
     grouped_gemm_w8a8_blockwise,
     is_weights_stats,
+    is_weights_stats_loss,
     last_error,
     quantize_act_gather,
     quantize_act_groupwise,

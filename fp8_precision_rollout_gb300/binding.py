@@ -68,6 +68,7 @@ def load(path: Optional[str] = None):
         "fp8rl_quantize_kv_fp8": (ctypes.c_int, [P, i64, i32, i32, i32, P, P, P]),
         "fp8rl_tis_weights": (ctypes.c_int, [P, P, P, i64, f32, f32, P, P]),
         "fp8rl_is_weights_stats": (ctypes.c_int, [P, P, P, i64, f32, f32, i32, P, P, P]),
+        "fp8rl_is_weights_stats_loss": (ctypes.c_int, [P, P, P, P, i64, f32, f32, i32, P, P, P]),
         "fp8rl_quantize_act_gather": (ctypes.c_int, [P, i64, i64, i64, P, i64, P, P, P]),
         "fp8rl_quantize_weights_blockwise_multi_host": (ctypes.c_int, [P, i32, P, ctypes.c_size_t,
                                                                        P]),
@@ -367,11 +368,13 @@ def tis_weights(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_lo: fl
 
 def is_weights_stats(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_lo: float = 0.0,
                      mode: int = FP8RL_IS_TRUNCATE, w: Optional[torch.Tensor] = None,
-                     stats: Optional[torch.Tensor] = None, weights: bool = True, stream=None):
+                     stats: Optional[torch.Tensor] = None, weights: bool = True, stream=None,
+                     loss: Optional[torch.Tensor] = None):
     """Importance weights (TIS or MIS by `mode`) and the batch's mismatch
     statistics [valid tokens, sum k1, sum k3, sum of ratios, clipped/masked
-    tokens] (float64 [5]).  weights=False computes the statistics only.
-    Returns (w or None, stats)."""
+    tokens] (float64 [5]); with a per-token `loss` (float32 [n]) a sixth entry,
+    the sum of fl32(w * loss) over the valid tokens.  weights=False computes
+    the statistics only.  Returns (w or None, stats)."""
     _dev(logp_train, torch.float32, "logp_train")
     _dev(logp_rollout, torch.float32, "logp_rollout")
     n = logp_train.numel()
@@ -385,17 +388,39 @@ def is_weights_stats(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_l
         wp = w.data_ptr()
     else:
         w = None
+    nstats = 5 if loss is None else 6
     if stats is None:
-        stats = torch.empty(5, dtype=torch.float64, device=logp_train.device)
+        stats = torch.empty(nstats, dtype=torch.float64, device=logp_train.device)
     _dev(stats, torch.float64, "stats")
+    if stats.numel() < nstats:
+        raise ValueError("stats must hold %d values" % nstats)
     mp = 0
     if mask is not None:
         _dev(mask, torch.uint8, "mask")
         mp = mask.data_ptr()
-    _check(load().fp8rl_is_weights_stats(logp_train.data_ptr(), logp_rollout.data_ptr(), mp, n,
-                                         float(c_hi), float(c_lo), int(mode), wp,
-                                         stats.data_ptr(), _stream(stream)))
+    if loss is None:
+        _check(load().fp8rl_is_weights_stats(logp_train.data_ptr(), logp_rollout.data_ptr(), mp, n,
+                                             float(c_hi), float(c_lo), int(mode), wp,
+                                             stats.data_ptr(), _stream(stream)))
+    else:
+        _dev(loss, torch.float32, "loss")
+        if loss.numel() != n:
+            raise ValueError("loss must have one value per token")
+        _check(load().fp8rl_is_weights_stats_loss(logp_train.data_ptr(), logp_rollout.data_ptr(),
+                                                  mp, loss.data_ptr(), n, float(c_hi),
+                                                  float(c_lo), int(mode), wp, stats.data_ptr(),
+                                                  _stream(stream)))
     return w, stats
+
+
+def is_weights_stats_loss(logp_train, logp_rollout, loss, mask=None, c_hi: float = 2.0,
+                          c_lo: float = 0.0, mode: int = FP8RL_IS_TRUNCATE,
+                          w: Optional[torch.Tensor] = None, stats: Optional[torch.Tensor] = None,
+                          weights: bool = True, stream=None):
+    """is_weights_stats with the importance-weighted token loss as a sixth
+    statistic (sum of fl32(w * loss) over the valid tokens)."""
+    return is_weights_stats(logp_train, logp_rollout, mask, c_hi, c_lo, mode, w, stats, weights,
+                            stream, loss=loss)
 
 
 def quantize_kv_fp8_calibrate_noalloc(x: torch.Tensor, scales: Optional[torch.Tensor] = None,

@@ -135,14 +135,15 @@ struct FF {
 // Running statistics of one thread: FP32 partial sums over the 8 tokens of a
 // round, folded into float-float sums after each round.
 struct IsAcc {
-  float k1 = 0.f, k3 = 0.f, r = 0.f;
-  FF K1, K3, R;
+  float k1 = 0.f, k3 = 0.f, r = 0.f, l = 0.f;
+  FF K1, K3, R, L;
   int nv = 0, nc = 0;
   __device__ __forceinline__ void fold() {
     K1.add(k1);
     K3.add(k3);
     R.add(r);
-    k1 = k3 = r = 0.f;
+    L.add(l);
+    k1 = k3 = r = l = 0.f;
   }
 };
 
@@ -157,11 +158,12 @@ __device__ __forceinline__ FF warp_sum(FF v) {
   return v;
 }
 
-// One token: weight by mode (0 = truncate, 1 = mask), statistics if valid.
+// One token: weight by mode (0 = truncate, 1 = mask), statistics if valid;
+// `loss` is the token's loss (0 when the call has none), weighted by w.
 template <int kMode>
-__device__ __forceinline__ float is_one(float lt, float lr, bool valid, float c_hi, float c_lo,
-                                        float th_lane, float tl_lane, const fx::Exp2Table& T,
-                                        IsAcc& acc) {
+__device__ __forceinline__ float is_one(float lt, float lr, float loss, bool valid, float c_hi,
+                                        float c_lo, float th_lane, float tl_lane,
+                                        const fx::Exp2Table& T, IsAcc& acc) {
   const float d = fx::fsub(lt, lr);
   const float e = tis_e(d, th_lane, tl_lane, T);
   float w;
@@ -182,20 +184,21 @@ __device__ __forceinline__ float is_one(float lt, float lr, bool valid, float c_
   acc.k1 = fx::fadd(acc.k1, fx::fsub(lr, lt));
   acc.k3 = fx::fadd(acc.k3, fx::fsub(fx::fsub(e, 1.0f), d));
   acc.r = fx::fadd(acc.r, e);
+  acc.l = fx::fadd(acc.l, fx::fmul(w, loss));
   acc.nv += 1;
   acc.nc += changed ? 1 : 0;
   return w;
 }
 
 template <int kMode>
-__device__ __forceinline__ float4 is_four(float4 a, float4 b, uint32_t valid4, float c_hi,
+__device__ __forceinline__ float4 is_four(float4 a, float4 b, float4 ls, uint32_t valid4, float c_hi,
                                           float c_lo, float th_lane, float tl_lane,
                                           const fx::Exp2Table& T, IsAcc& acc) {
   float4 r;
-  r.x = is_one<kMode>(a.x, b.x, valid4 & 1u, c_hi, c_lo, th_lane, tl_lane, T, acc);
-  r.y = is_one<kMode>(a.y, b.y, valid4 & 2u, c_hi, c_lo, th_lane, tl_lane, T, acc);
-  r.z = is_one<kMode>(a.z, b.z, valid4 & 4u, c_hi, c_lo, th_lane, tl_lane, T, acc);
-  r.w = is_one<kMode>(a.w, b.w, valid4 & 8u, c_hi, c_lo, th_lane, tl_lane, T, acc);
+  r.x = is_one<kMode>(a.x, b.x, ls.x, valid4 & 1u, c_hi, c_lo, th_lane, tl_lane, T, acc);
+  r.y = is_one<kMode>(a.y, b.y, ls.y, valid4 & 2u, c_hi, c_lo, th_lane, tl_lane, T, acc);
+  r.z = is_one<kMode>(a.z, b.z, ls.z, valid4 & 4u, c_hi, c_lo, th_lane, tl_lane, T, acc);
+  r.w = is_one<kMode>(a.w, b.w, ls.w, valid4 & 8u, c_hi, c_lo, th_lane, tl_lane, T, acc);
   return r;
 }
 
@@ -209,15 +212,17 @@ __device__ __forceinline__ uint32_t valid_bits(const uint8_t* __restrict__ mask,
 }
 
 // Same traversal as tis_kernel; the statistics are reduced per CTA and added
-// to stats[5] (cleared beforehand) with one FP64 atomic each.
+// to stats[nstats] (cleared beforehand) with one FP64 atomic each; nstats = 6
+// adds the loss-weighted sum (loss non-null), 5 otherwise.
 template <int kMode, bool kW, int V>
 __global__ void __launch_bounds__(256) is_stats_kernel(const float* __restrict__ lt,
                                                        const float* __restrict__ lr,
-                                                       const uint8_t* __restrict__ mask, int64_t n,
+                                                       const uint8_t* __restrict__ mask,
+                                                       const float* __restrict__ loss, int64_t n,
                                                        float c_hi, float c_lo, float* __restrict__ w,
-                                                       double* __restrict__ stats,
+                                                       double* __restrict__ stats, int nstats,
                                                        const __grid_constant__ fx::Exp2Table T) {
-  __shared__ double red[8][5];
+  __shared__ double red[8][6];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float th_lane = T.hi[lane];
   const float tl_lane = T.lo[lane];
@@ -226,25 +231,27 @@ __global__ void __launch_bounds__(256) is_stats_kernel(const float* __restrict__
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const float4* lt4 = reinterpret_cast<const float4*>(lt);
   const float4* lr4 = reinterpret_cast<const float4*>(lr);
+  const float4* ls4 = reinterpret_cast<const float4*>(loss);
   IsAcc acc;
   for (int64_t v0 = gw * (32 * V); v0 < n4; v0 += nwarps * (32 * V)) {
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 a[V], b[V];
+    float4 a[V], b[V], l4[V];
     uint32_t mb[V];
 #pragma unroll
     for (int u = 0; u < V; ++u) {
       const int64_t i = v0 + lane + 32 * u;
       a[u] = i < n4 ? __ldg(lt4 + i) : z;
       b[u] = i < n4 ? __ldg(lr4 + i) : z;
+      l4[u] = (loss && i < n4) ? __ldg(ls4 + i) : z;
       mb[u] = valid_bits(mask, i, i < n4);
     }
 #pragma unroll
     for (int u = 0; u < V; ++u) {
       const int64_t i = v0 + lane + 32 * u;
-      const float4 r = is_four<kMode>(a[u], b[u], mb[u], c_hi, c_lo, th_lane, tl_lane, T, acc);
+      const float4 r = is_four<kMode>(a[u], b[u], l4[u], mb[u], c_hi, c_lo, th_lane, tl_lane, T, acc);
       if (kW && i < n4) reinterpret_cast<float4*>(w)[i] = r;
+      if ((u & 1) || u == V - 1) acc.fold();   // FP32 partials over at most 8 tokens
     }
-    acc.fold();
   }
   // ragged tail (n % 4 tokens): the first warp of block 0
   const int64_t tail = n - (n4 << 2);
@@ -252,8 +259,8 @@ __global__ void __launch_bounds__(256) is_stats_kernel(const float* __restrict__
     const int64_t j = (n4 << 2) + lane;
     const bool in = lane < tail;
     const bool valid = in && (!mask || mask[j]);
-    const float r = is_one<kMode>(in ? lt[j] : 0.f, in ? lr[j] : 0.f, valid, c_hi, c_lo, th_lane,
-                                  tl_lane, T, acc);
+    const float r = is_one<kMode>(in ? lt[j] : 0.f, in ? lr[j] : 0.f, (loss && in) ? loss[j] : 0.f,
+                                  valid, c_hi, c_lo, th_lane, tl_lane, T, acc);
     acc.fold();
     if (kW && in) w[j] = r;
   }
@@ -264,15 +271,17 @@ __global__ void __launch_bounds__(256) is_stats_kernel(const float* __restrict__
     nc += __shfl_xor_sync(0xFFFFFFFFu, nc, o);
   }
   const FF k1 = warp_sum(acc.K1), k3 = warp_sum(acc.K3), rr = warp_sum(acc.R);
+  const FF ll = warp_sum(acc.L);
   if (lane == 0) {
     red[warp][0] = (double)nv;
     red[warp][1] = k1.value();
     red[warp][2] = k3.value();
     red[warp][3] = rr.value();
     red[warp][4] = (double)nc;
+    red[warp][5] = ll.value();
   }
   __syncthreads();
-  if (threadIdx.x < 5) {
+  if ((int)threadIdx.x < nstats) {
     double t = 0.0;
     for (int k = 0; k < (int)(blockDim.x >> 5); ++k) t += red[k][threadIdx.x];
     atomicAdd(stats + threadIdx.x, t);
@@ -300,8 +309,8 @@ WaveFit fit_wave(int64_t n, int sms, const int per_sm[3]) {
 
 template <int kMode, bool kW>
 void launch_is_stats_v(int sms, cudaStream_t stream, const float* lt, const float* lr,
-                       const uint8_t* mask, int64_t n, float c_hi, float c_lo, float* w,
-                       double* stats, const fx::Exp2Table& T) {
+                       const uint8_t* mask, const float* loss, int64_t n, float c_hi, float c_lo,
+                       float* w, double* stats, int nstats, const fx::Exp2Table& T) {
   static const int per_sm[3] = {resident_ctas_per_sm(is_stats_kernel<kMode, kW, 2>, 256),
                                 resident_ctas_per_sm(is_stats_kernel<kMode, kW, 3>, 256),
                                 resident_ctas_per_sm(is_stats_kernel<kMode, kW, 4>, 256)};
@@ -309,22 +318,30 @@ void launch_is_stats_v(int sms, cudaStream_t stream, const float* lt, const floa
   const int v = f.v;
   const unsigned grid = (unsigned)f.ctas;
   if (v == 2)
-    is_stats_kernel<kMode, kW, 2><<<grid, 256, 0, stream>>>(lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+    is_stats_kernel<kMode, kW, 2><<<grid, 256, 0, stream>>>(lt, lr, mask, loss, n, c_hi, c_lo, w,
+                                                            stats, nstats, T);
   else if (v == 3)
-    is_stats_kernel<kMode, kW, 3><<<grid, 256, 0, stream>>>(lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+    is_stats_kernel<kMode, kW, 3><<<grid, 256, 0, stream>>>(lt, lr, mask, loss, n, c_hi, c_lo, w,
+                                                            stats, nstats, T);
   else
-    is_stats_kernel<kMode, kW, 4><<<grid, 256, 0, stream>>>(lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+    is_stats_kernel<kMode, kW, 4><<<grid, 256, 0, stream>>>(lt, lr, mask, loss, n, c_hi, c_lo, w,
+                                                            stats, nstats, T);
 }
 
 void launch_is_stats(int32_t mode, bool with_w, int sms, cudaStream_t stream, const float* lt,
-                     const float* lr, const uint8_t* mask, int64_t n, float c_hi, float c_lo,
-                     float* w, double* stats, const fx::Exp2Table& T) {
+                     const float* lr, const uint8_t* mask, const float* loss, int64_t n,
+                     float c_hi, float c_lo, float* w, double* stats, int nstats,
+                     const fx::Exp2Table& T) {
   if (mode == FP8RL_IS_TRUNCATE) {
-    if (with_w) launch_is_stats_v<0, true>(sms, stream, lt, lr, mask, n, c_hi, c_lo, w, stats, T);
-    else launch_is_stats_v<0, false>(sms, stream, lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+    if (with_w)
+      launch_is_stats_v<0, true>(sms, stream, lt, lr, mask, loss, n, c_hi, c_lo, w, stats, nstats, T);
+    else
+      launch_is_stats_v<0, false>(sms, stream, lt, lr, mask, loss, n, c_hi, c_lo, w, stats, nstats, T);
   } else {
-    if (with_w) launch_is_stats_v<1, true>(sms, stream, lt, lr, mask, n, c_hi, c_lo, w, stats, T);
-    else launch_is_stats_v<1, false>(sms, stream, lt, lr, mask, n, c_hi, c_lo, w, stats, T);
+    if (with_w)
+      launch_is_stats_v<1, true>(sms, stream, lt, lr, mask, loss, n, c_hi, c_lo, w, stats, nstats, T);
+    else
+      launch_is_stats_v<1, false>(sms, stream, lt, lr, mask, loss, n, c_hi, c_lo, w, stats, nstats, T);
   }
 }
 
@@ -363,29 +380,49 @@ extern "C" fp8rl_status fp8rl_tis_weights(const float* logp_train, const float* 
   return st == FP8RL_OK ? ok() : st;
 }
 
-extern "C" fp8rl_status fp8rl_is_weights_stats(const float* logp_train, const float* logp_rollout,
-                                               const uint8_t* mask, int64_t n, float c_hi,
-                                               float c_lo, int32_t mode, float* w, double* stats,
-                                               cudaStream_t stream) {
+namespace {
+fp8rl_status is_stats_call(const float* logp_train, const float* logp_rollout, const uint8_t* mask,
+                           const float* loss, int64_t n, float c_hi, float c_lo, int32_t mode,
+                           float* w, double* stats, int nstats, cudaStream_t stream) {
   if (!stats || (n > 0 && (!logp_train || !logp_rollout)))
     return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (nstats == 6 && n > 0 && !loss) return fail(FP8RL_ERR_INVALID_ARG, "null loss");
   if (n < 0) return fail(FP8RL_ERR_INVALID_ARG, "n must be >= 0");
   if (mode != FP8RL_IS_TRUNCATE && mode != FP8RL_IS_MASK)
     return fail(FP8RL_ERR_INVALID_ARG, "mode must be FP8RL_IS_TRUNCATE or FP8RL_IS_MASK");
   if (!(c_hi > 0.0f) || !std::isfinite(c_hi) || !(c_lo >= 0.0f) || !(c_lo <= c_hi))
     return fail(FP8RL_ERR_INVALID_ARG, "need 0 <= c_lo <= c_hi, c_hi finite and > 0");
   if (!aligned(logp_train, 16) || !aligned(logp_rollout, 16) || (w && !aligned(w, 16)) ||
-      (mask && !aligned(mask, 4)) || !aligned(stats, 8))
+      (mask && !aligned(mask, 4)) || (loss && !aligned(loss, 16)) || !aligned(stats, 8))
     return fail(FP8RL_ERR_ALIGNMENT,
-                "log-prob and weight arrays must be 16-byte aligned, mask 4-byte, stats 8-byte");
+                "log-prob, loss and weight arrays must be 16-byte aligned, mask 4-byte, stats 8-byte");
   DeviceState* ds = nullptr;
   fp8rl_status st = device_state(&ds);
   if (st != FP8RL_OK) return st;
-  st = cuda_check(cudaMemsetAsync(stats, 0, 5 * sizeof(double), stream), "cudaMemsetAsync(stats)");
+  st = cuda_check(cudaMemsetAsync(stats, 0, (size_t)nstats * sizeof(double), stream),
+                  "cudaMemsetAsync(stats)");
   if (st != FP8RL_OK || n == 0) return st == FP8RL_OK ? ok() : st;
   static const fx::Exp2Table T = fx::make_exp_tables();
-  launch_is_stats(mode, w != nullptr, ds->sm_count, stream, logp_train, logp_rollout, mask, n,
-                  c_hi, c_lo, w, stats, T);
+  launch_is_stats(mode, w != nullptr, ds->sm_count, stream, logp_train, logp_rollout, mask,
+                  nstats == 6 ? loss : nullptr, n, c_hi, c_lo, w, stats, nstats, T);
   st = cuda_check(cudaGetLastError(), "is_stats_kernel launch");
   return st == FP8RL_OK ? ok() : st;
+}
+}  // namespace
+
+extern "C" fp8rl_status fp8rl_is_weights_stats(const float* logp_train, const float* logp_rollout,
+                                               const uint8_t* mask, int64_t n, float c_hi,
+                                               float c_lo, int32_t mode, float* w, double* stats,
+                                               cudaStream_t stream) {
+  return is_stats_call(logp_train, logp_rollout, mask, nullptr, n, c_hi, c_lo, mode, w, stats, 5,
+                       stream);
+}
+
+extern "C" fp8rl_status fp8rl_is_weights_stats_loss(const float* logp_train,
+                                                    const float* logp_rollout, const uint8_t* mask,
+                                                    const float* loss, int64_t n, float c_hi,
+                                                    float c_lo, int32_t mode, float* w,
+                                                    double* stats, cudaStream_t stream) {
+  return is_stats_call(logp_train, logp_rollout, mask, loss, n, c_hi, c_lo, mode, w, stats, 6,
+                       stream);
 }

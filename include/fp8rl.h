@@ -318,6 +318,21 @@ fp8rl_status fp8rl_is_weights_stats(const float* logp_train, const float* logp_r
                                     const uint8_t* mask, int64_t n, float c_hi, float c_lo,
                                     int32_t mode, float* w, double* stats, cudaStream_t stream);
 
+/* fp8rl_is_weights_stats plus the importance-weighted token loss (section
+ * 3.4.3: token-level TIS multiplies each token's policy-gradient loss by its
+ * truncated weight).  With loss[i] the caller's per-token loss, stats[0..4]
+ * are as above and
+ *   stats[5]  sum over the valid tokens of fl32(w * loss)  (divide by
+ *             stats[0] for the token mean)
+ * accumulated like the other sums (within 2^-20 * sum of |terms|).
+ *   loss     FP32 [n] (device), 16-byte aligned; may be NULL only when n == 0
+ *   stats    FP64 [6], 8-byte aligned, overwritten (cleared on `stream` first)
+ * Other arguments and errors as in fp8rl_is_weights_stats. */
+fp8rl_status fp8rl_is_weights_stats_loss(const float* logp_train, const float* logp_rollout,
+                                         const uint8_t* mask, const float* loss, int64_t n,
+                                         float c_hi, float c_lo, int32_t mode, float* w,
+                                         double* stats, cudaStream_t stream);
+
 /* Synchronizes the device and returns FP8RL_ERR_TIMEOUT if any kernel since
  * the last clear hit a device-side wait limit, FP8RL_ERR_INVALID_ARG if a
  * kernel met an out-of-range device-side index (fp8rl_quantize_act_gather,

@@ -418,7 +418,7 @@ def _sum64(x: np.ndarray) -> float:
 
 
 def is_weights_stats(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_lo: float = 0.0,
-                     mode: int = IS_TRUNCATE):
+                     mode: int = IS_TRUNCATE, loss=None):
     """Importance weights of one batch with their mismatch statistics.
 
     Summary page, section 3.4.3: the weight w = pi_theta / pi_fp8 =
@@ -439,6 +439,10 @@ def is_weights_stats(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_l
       stats[4] = number of valid tokens whose weight was clipped (TIS) or
                  masked to 0 (MIS).
       Sums are returned (not means) so that batches can be combined.
+    * with a per-token loss l (the trainer's policy-gradient loss of each
+      token; section 3.4.3 multiplies it by the truncated weight in token-level
+      TIS), stats[5] = sum over the valid tokens of fl32(w * l): the
+      importance-weighted token loss (divide by stats[0] for its mean).
     """
     lt = np.asarray(logp_train, dtype=np.float32).reshape(-1)
     lr = np.asarray(logp_rollout, dtype=np.float32).reshape(-1)
@@ -465,6 +469,10 @@ def is_weights_stats(logp_train, logp_rollout, mask=None, c_hi: float = 2.0, c_l
                       float((changed & valid).sum())], dtype=np.float64)
     terms_abs = np.array([0.0, _sum64(np.abs(k1[valid])), _sum64(np.abs(k3[valid])),
                           _sum64(np.abs(e[valid])), 0.0])
+    if loss is not None:
+        lw = (w * np.asarray(loss, dtype=np.float32).reshape(-1)).astype(np.float32)
+        stats = np.append(stats, _sum64(lw[valid]))
+        terms_abs = np.append(terms_abs, _sum64(np.abs(lw[valid])))
     return w, stats, terms_abs
 
 

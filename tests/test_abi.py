@@ -19,7 +19,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     declared = binding.declared_symbols()
-    assert len(declared) == 16
+    assert len(declared) == 17
     for name in declared:
         assert hasattr(lib, name), name
     # and the binding wraps each of them under the same name

@@ -81,18 +81,21 @@ def test_every_binary32_log_ratio():
 # ------------------------------------------------ IS weights + mismatch stats --
 
 def _stats_case(lt, lr, dev, mask=None, c_hi=2.0, c_lo=0.0, mode=fp8rl.FP8RL_IS_TRUNCATE,
-                weights=True):
+                weights=True, loss=None):
     n = lt.numel()
+    nst = 5 if loss is None else 6
     wc = Canary(max(n, 1), torch.float32, dev)
-    sc = Canary(5, torch.float64, dev)
+    sc = Canary(nst, torch.float64, dev)
     w, st = fp8rl.is_weights_stats(lt.to(dev), lr.to(dev), None if mask is None else mask.to(dev),
                                    c_hi, c_lo, mode, w=wc.view[:n] if weights else None,
-                                   stats=sc.view, weights=weights)
+                                   stats=sc.view, weights=weights,
+                                   loss=None if loss is None else loss.to(dev))
     torch.cuda.synchronize()
     wc.check(); sc.check()
     ref_w, ref_st, terms_abs = oracle.is_weights_stats(lt.numpy(), lr.numpy(),
                                                        None if mask is None else mask.numpy(),
-                                                       c_hi, c_lo, mode)
+                                                       c_hi, c_lo, mode,
+                                                       None if loss is None else loss.numpy())
     if weights:
         got = w.cpu().numpy()
         same = (got.view(np.uint32) == ref_w.view(np.uint32)) | (np.isnan(got) & np.isnan(ref_w))
@@ -102,7 +105,7 @@ def _stats_case(lt, lr, dev, mask=None, c_hi=2.0, c_lo=0.0, mode=fp8rl.FP8RL_IS_
     g = st.cpu().numpy()
     # counts exact; sums within the documented bound 2^-20 * sum |terms|
     assert g[0] == ref_st[0] and g[4] == ref_st[4]
-    for q in (1, 2, 3):
+    for q in ((1, 2, 3) if loss is None else (1, 2, 3, 5)):
         if not np.isfinite(ref_st[q]):   # inf / NaN terms propagate
             assert g[q] == ref_st[q] or (np.isnan(g[q]) and np.isnan(ref_st[q])), (q, g[q])
             continue
@@ -152,3 +155,20 @@ def test_is_stats_special_values_and_empty():
     torch.cuda.synchronize()
     sc.check()
     assert (sc.view.cpu().numpy() == 0).all()
+
+
+@pytest.mark.parametrize("mode", [fp8rl.FP8RL_IS_TRUNCATE, fp8rl.FP8RL_IS_MASK])
+def test_is_stats_weighted_loss(mode):
+    """The importance-weighted token loss (sixth statistic) on ragged sizes, with
+    and without a mask, and on the long-context Student-t workload."""
+    dev = device()
+    for n in (1, 5, 4096, 4099, 70001):
+        lt, lr = workloads.tis_logprobs(n, seed=100 + n)
+        loss = torch.randn(n, generator=torch.Generator().manual_seed(n))
+        _stats_case(lt, lr, dev, mode=mode, loss=loss)
+        mask = (torch.arange(n) % 3 != 1).to(torch.uint8)
+        _stats_case(lt, lr, dev, mask=mask, mode=mode, c_lo=0.5, loss=loss)
+    lt, lr = workloads.tis_logprobs(64 * 20480, seed=5, kind="student_t")
+    loss = torch.randn(lt.numel(), generator=torch.Generator().manual_seed(9)).abs_()
+    g, ref = _stats_case(lt, lr, dev, mode=mode, loss=loss, weights=False)
+    assert len(g) == 6

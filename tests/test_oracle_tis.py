@@ -164,3 +164,31 @@ def test_is_stats_estimate_kl_of_gaussian_shift():
     k3 = ((e - np.float32(1)).astype(np.float32) - (lt - lr).astype(np.float32)).astype(np.float32)
     big = np.abs((lt - lr).astype(np.float32)) >= 2.0 ** -9
     assert (k3[big] > 0).all()
+
+
+def test_is_stats_weighted_loss_closed_forms():
+    """Sixth statistic, sum of fl32(w * loss) over the valid tokens: lt == lr gives
+    w = 1 (the plain loss sum); d >= ln 2 gives w = 2 under TIS and 0 under MIS;
+    masked-out tokens never count; one token is the product itself."""
+    rng = np.random.default_rng(41)
+    n = 999
+    lt = rng.uniform(-20, -0.1, n).astype(np.float32)
+    loss = rng.normal(0, 1, n).astype(np.float32)
+    _, st, ta = oracle.is_weights_stats(lt, lt.copy(), loss=loss)
+    assert len(st) == 6 and st[5] == math.fsum(loss.astype(np.float64).tolist())
+    assert ta[5] == math.fsum(np.abs(loss).astype(np.float64).tolist())
+    lr = (lt - np.float32(1.0)).astype(np.float32)            # d = 1 > ln 2 for every token
+    assert ((lt - lr).astype(np.float32) >= np.float32(0.6932)).all()
+    _, st, _ = oracle.is_weights_stats(lt, lr, loss=loss)
+    assert st[5] == math.fsum((2.0 * loss.astype(np.float64)).tolist())
+    _, st, _ = oracle.is_weights_stats(lt, lr, loss=loss, mode=oracle.IS_MASK)
+    assert st[5] == 0.0
+    mask = (np.arange(n) % 4 == 0).astype(np.uint8)
+    _, st, _ = oracle.is_weights_stats(lt, lt.copy(), mask=mask, loss=loss)
+    assert st[5] == math.fsum(loss[mask == 1].astype(np.float64).tolist())
+    # one token: the rounded product of its weight and loss
+    w, st, _ = oracle.is_weights_stats(lt[:1], (lt[:1] + np.float32(0.3)).astype(np.float32),
+                                       loss=np.float32([3.0]))
+    assert st[5] == float(np.float32(w[0] * np.float32(3.0)))
+    # without a loss the statistics keep five entries
+    assert len(oracle.is_weights_stats(lt, lt.copy())[1]) == 5
