@@ -224,7 +224,9 @@ class Workload:
         self.lt, self.lr = wl.tis_logprobs(64 * 20480, seed=5, device=dev, kind="student_t")
         self.tw = torch.empty_like(self.lt)
         self.mw = torch.empty_like(self.lt)
-        self.is_stats = torch.empty(5, dtype=torch.float64, device=dev)
+        # the trainer's per-token loss, weighted by the MIS weights in the same pass
+        self.tok_loss = torch.randn(self.lt.numel(), generator=torch.Generator().manual_seed(8)).to(dev)
+        self.is_stats = torch.empty(6, dtype=torch.float64, device=dev)
         torch.cuda.synchronize()
 
     # one step; records an event pair around each row on the current stream
@@ -275,7 +277,7 @@ class Workload:
         launches += 1
         mark("tis_end")
         fp8rl.is_weights_stats(self.lt, self.lr, None, 2.0, 0.5, fp8rl.FP8RL_IS_MASK, w=self.mw,
-                               stats=self.is_stats)
+                               stats=self.is_stats, loss=self.tok_loss)
         launches += 1
         mark("is_end")
         return launches
@@ -343,9 +345,10 @@ def _rows(W, ev, steps, peaks):
     out["a6_tis"] = {"ms": t, "bytes": tb, "gbs": tb / t / 1e6, "frac_hbm": tb / t / 1e6 / hbm,
                      "note": "instruction-issue and launch bound at this size"}
     t = statistics.mean(_ms(ev, "tis_end", "is_end"))
-    out["a6b_mis_stats"] = {"ms": t, "tokens": W.lt.numel(), "bytes": tb,
-                            "gbs": tb / t / 1e6, "frac_hbm": tb / t / 1e6 / hbm,
-                            "note": "MIS weights + mismatch statistics, one pass"}
+    mb = 16 * W.lt.numel()   # two log-probs and the loss read, the weight written
+    out["a6b_mis_stats"] = {"ms": t, "tokens": W.lt.numel(), "bytes": mb,
+                            "gbs": mb / t / 1e6, "frac_hbm": mb / t / 1e6 / hbm,
+                            "note": "MIS weights + mismatch statistics + weighted token loss, one pass"}
     return out
 
 
