@@ -132,6 +132,32 @@ def test_weight_quant_shapes(n, k):
     _wq_case(workloads.make_weight(n, k, seed=n + 3 * k), dev)
 
 
+def test_weight_quant_special_values():
+    """One pattern per 128x128 block: zeros of both signs (scale 0), the
+    smallest subnormals, BF16 max, subnormals only, exactly 1.0, values near
+    1e-20 (a scale below 2^-60: the IEEE-division branch), one outlier among
+    tiny values; random finite bit patterns elsewhere; then a ragged copy."""
+    dev = device()
+    rng = np.random.default_rng(17)
+    bits = rng.integers(0, 1 << 16, size=(384, 512)).astype(np.uint16)
+    bits[(bits & 0x7F80) == 0x7F80] &= 0xBFFF          # no inf/NaN (out of contract)
+    blk = lambda i, j: (slice(128 * i, 128 * i + 128), slice(128 * j, 128 * j + 128))  # noqa: E731
+    bits[blk(0, 0)] = 0
+    bits[blk(0, 1)] = 0x8000
+    bits[blk(0, 2)] = 0x0001
+    b = bits[blk(0, 3)]; b[::3, ::5] = 0x7F7F; b[1::3, ::5] = 0xFF7F
+    bits[blk(1, 0)] = rng.integers(0, 0x80, size=(128, 128)) | (rng.integers(0, 2, size=(128, 128)) << 15)
+    bits[blk(1, 1)] = 0x3F80
+    tiny = (rng.normal(0, 1, size=(128, 128)) * 1e-20).astype(np.float32)
+    bits[blk(1, 2)] = (tiny.view(np.uint32) >> 16).astype(np.uint16)
+    small = (rng.normal(0, 1, size=(128, 128)) * 1e-3).astype(np.float32)
+    small[77, 3] = -250.0
+    bits[blk(1, 3)] = (small.view(np.uint32) >> 16).astype(np.uint16)
+    w = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    _wq_case(w, dev)
+    _wq_case(w[:300, :520].contiguous(), dev)
+
+
 def test_weight_quant_strides():
     dev = device()
     _wq_case(workloads.make_weight(300, 520, seed=9), dev, ldw_pad=40, ldq_pad=24)
@@ -180,7 +206,8 @@ def test_requant_qwen3_8b_full_model_sampled():
 
 
 @pytest.mark.parametrize("seqs,tokens,heads,hd", [(2, 37, 8, 128), (1, 1, 8, 128), (3, 50, 4, 64),
-                                                  (2, 9, 2, 8), (1, 5, 1, 2048), (4, 300, 16, 128)])
+                                                  (2, 9, 2, 8), (1, 5, 1, 2048), (4, 300, 16, 128),
+                                                  (2, 11, 256, 8)])
 def test_kv_calibrate_and_given(seqs, tokens, heads, hd):
     dev = device()
     x = workloads.kv_tensor(seed=seqs * tokens, seqs=seqs, tokens=tokens, heads=heads, head_dim=hd)
