@@ -157,12 +157,13 @@ FP8RL_HD void two_prod(float a, float b, float& p, float& e) {
   e = ffma(a, b, -p);
 }
 
-// Fast path, in two parts so that a caller can fetch the table entry its own
-// way (the CUDA kernel takes it from lane registers with a warp shuffle):
-// exp_fast_index() gives the table index j of d (any d, also out of range),
-// exp_rn32_fast_with() finishes with th + tl = 2^(j/32).  It returns false
-// when the input must take exp_rn32_slow (|d| > 87, NaN, or a result too close
-// to a rounding boundary to decide here).
+// Fast path, in parts so that a caller can fetch the table entry its own way
+// (the CUDA kernel takes it from lane registers with a warp shuffle):
+// exp_fast_k() gives the reduction multiple kf of d, exp_fast_index_k() the
+// table index j (any d, also out of range), and exp_rn32_fast_with_k()
+// finishes with th + tl = 2^(j/32).  It returns false when the input must
+// take exp_rn32_slow (|d| > 87, NaN, or a result too close to a rounding
+// boundary to decide here).
 // ln2/32 is split in three: L1 has 12 significant bits so that k*L1 is exact
 // for |k| < 2^12; L2 and L3 carry the next 48 bits.
 constexpr float kExpInvL = 0x1.715476p+5f;      // ~32/ln2; only sets the reduction range
@@ -177,9 +178,7 @@ FP8RL_HD int exp_fast_index_k(float kf) {
   return fabsf(kf) < 65536.0f ? (((int)kf) & 31) : 0;   // out-of-range d: any valid index
 }
 
-FP8RL_HD int exp_fast_index(float d) { return exp_fast_index_k(exp_fast_k(d)); }
-
-// As exp_rn32_fast_with below, given kf = exp_fast_k(d).
+// e^d rounded to binary32, or false (see above); kf = exp_fast_k(d).
 FP8RL_HD bool exp_rn32_fast_with_k(float d, float kf, float th, float tl, float* out) {
   if (!(fabsf(d) <= 87.0f)) return false;
   int k = (int)kf;
@@ -222,15 +221,6 @@ FP8RL_HD bool exp_rn32_fast_with_k(float d, float kf, float th, float tl, float*
   if (dist <= fmul(yh, 0x1p-40f)) return false;
   *out = fmul(yh, u2f((uint32_t)(m + 127) << 23));   // exact: the result is normal
   return true;
-}
-
-FP8RL_HD bool exp_rn32_fast_with(float d, float th, float tl, float* out) {
-  return exp_rn32_fast_with_k(d, exp_fast_k(d), th, tl, out);
-}
-
-FP8RL_HD bool exp_rn32_fast(float d, const Exp2Table& T, float* out) {
-  const int j = exp_fast_index(d);
-  return exp_rn32_fast_with(d, T.hi[j], T.lo[j], out);
 }
 
 // double-double helpers for the slow path
@@ -303,12 +293,6 @@ FP8RL_HD_OUTLINE float exp_rn32_slow(float d, const Exp2Table& T) {
   e = dd_fast(e.hi, dadd(e.lo, dadd(r.lo, dfma(rh, r.lo, q))));
   const dd v = dd_mul(e, dd{T.dhi[j], T.dlo[j]});
   return dd_round_to_float(ldexp(v.hi, m), ldexp(v.lo, m));
-}
-
-FP8RL_HD float exp_rn32(float d, const Exp2Table& T) {
-  float e;
-  if (exp_rn32_fast(d, T, &e)) return e;
-  return exp_rn32_slow(d, T);
 }
 
 // Host-side construction of the tables.  2^(j/32) = e^(j ln2/32) is formed
