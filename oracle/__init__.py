@@ -59,7 +59,6 @@ def lib():
         L.orc_e4m3_decode_array.argtypes = [P, P, i64]
         L.orc_quantize_values.argtypes = [P, P, P, i64, ctypes.c_int]
         L.orc_quantize_weights_blockwise.argtypes = [P, i64, i64, i64, P, i64, P, ctypes.c_int]
-        L.orc_quantize_weight_blocks.argtypes = [P, i64, i64, i64, P, i64, P, P]
         L.orc_quantize_act_groupwise.argtypes = [P, i64, i64, i64, P, P, ctypes.c_int]
         L.orc_kv_calibrate.argtypes = [P, i64, ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
         L.orc_kv_quantize.argtypes = [P, i64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int]
@@ -135,20 +134,6 @@ def quantize_weights_blockwise(w):
     q = np.zeros((n, k), dtype=np.uint8)
     s = np.zeros(((n + 127) // 128, (k + 127) // 128), dtype=np.float32)
     lib().orc_quantize_weights_blockwise(_p(wb), n, k, k, _p(q), k, _p(s), threads())
-    return q, s
-
-
-def quantize_weight_blocks(w, block_ids):
-    """The same map on selected blocks only (row-major block ids).
-
-    Returns (codes uint8 [len(ids), 128, 128] zero-padded, scales float32 [len(ids)]).
-    """
-    wb = _u16(w)
-    n, k = wb.shape
-    ids = np.ascontiguousarray(np.asarray(block_ids, dtype=np.int64))
-    q = np.zeros((ids.size, 128, 128), dtype=np.uint8)
-    s = np.zeros(ids.size, dtype=np.float32)
-    lib().orc_quantize_weight_blocks(_p(wb), n, k, k, _p(ids), ids.size, _p(q), _p(s))
     return q, s
 
 

@@ -225,31 +225,6 @@ void orc_quantize_weights_blockwise(const uint16_t* w, int64_t n, int64_t k,
   });
 }
 
-// Same map, restricted to a list of blocks (used to check full-size launches
-// on sampled blocks).  block_ids index the row-major block grid.
-void orc_quantize_weight_blocks(const uint16_t* w, int64_t n, int64_t k,
-                                int64_t ldw, const int64_t* block_ids,
-                                int64_t nblocks, uint8_t* q_blocks /*[nblocks,128,128]*/,
-                                float* s_blocks) {
-  int64_t kb = (k + 127) / 128;
-  for (int64_t t = 0; t < nblocks; ++t) {
-    int64_t bi = block_ids[t] / kb, bj = block_ids[t] % kb;
-    int64_t i0 = bi * 128, i1 = std::min(n, i0 + 128);
-    int64_t j0 = bj * 128, j1 = std::min(k, j0 + 128);
-    float amax = 0.0f;
-    for (int64_t i = i0; i < i1; ++i)
-      for (int64_t j = j0; j < j1; ++j)
-        amax = std::max(amax, std::fabs(bf16_to_float(w[i * ldw + j])));
-    float s = scale_from_amax(amax);
-    s_blocks[t] = s;
-    uint8_t* out = q_blocks + t * 128 * 128;
-    std::memset(out, 0, 128 * 128);
-    for (int64_t i = i0; i < i1; ++i)
-      for (int64_t j = j0; j < j1; ++j)
-        out[(i - i0) * 128 + (j - j0)] = quantize_one(bf16_to_float(w[i * ldw + j]), s);
-  }
-}
-
 // ------------------------------------------------ 1x128 activation groups --
 // [S341] (1x128 activation tiles, after DeepSeek-V3) and the dynamic
 // activation quantization of [S342] Phase 3: per token, per 128-wide group of
