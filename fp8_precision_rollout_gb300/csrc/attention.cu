@@ -581,11 +581,25 @@ int attn_active_clusters(const DeviceState* ds, int c) {
 // wave and every rank keeps at least two stages per consumer warp.
 template <bool kSwz>
 int choose_csplit(const DeviceState* ds, int64_t pairs, int64_t nst_cap) {
+  // resident CTAs per SM, queried once per device (not on every launch, so
+  // that a launch under CUDA-graph capture makes no occupancy query)
+  static int cache[64] = {};
+  static std::mutex mu;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<kSwz>,
-                                                    kAttnThreads, kAttnSmem) != cudaSuccess) {
-    (void)cudaGetLastError();
-    per_sm = 1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    int* slot = ds->device < 64 ? &cache[ds->device] : nullptr;
+    if (slot && *slot) {
+      per_sm = *slot;
+    } else {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<kSwz>,
+                                                        kAttnThreads, kAttnSmem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        per_sm = 1;
+      }
+      per_sm = std::max(per_sm, 1);
+      if (slot) *slot = per_sm;
+    }
   }
   const int64_t slots = (int64_t)ds->sm_count * std::max(per_sm, 1);
   int c = 1;
