@@ -132,8 +132,8 @@ struct FF {
   __device__ __forceinline__ double value() const { return (double)hi + (double)lo; }
 };
 
-// Running statistics of one thread: FP32 partial sums over the 8 tokens of a
-// round, folded into float-float sums after each round.
+// Running statistics of one thread: FP32 partial sums over at most 8 tokens
+// (two 4-token vectors), then folded into float-float sums.
 struct IsAcc {
   float k1 = 0.f, k3 = 0.f, r = 0.f, l = 0.f;
   FF K1, K3, R, L;
