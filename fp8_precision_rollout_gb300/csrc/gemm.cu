@@ -19,7 +19,7 @@
 // Kernel shape (one CTA per SM, persistent over output tiles):
 //   tile 128 (M) x 256 (N), k-block 128; TMA ring of 48 KB stages (A 128x128
 //   + B 256x128 bytes, 128-byte swizzle), 3 stages plus 64 KB of output
-//   staging, or 4 stages in the split-K flavour;
+//   staging.  The split-K flavour uses 128 x 128 tiles and 6 stages of 32 KB;
 //   warp 0      TMA producer (lane 0),
 //   warps 1, 2  MMA issuers (tcgen05.mma kind::f8f6f4, M=128 N=256 K=32, four
 //               per k-block, lane 0): warp 1 issues the even k-blocks into
@@ -29,14 +29,16 @@
 //               spends executing it; two alternating issuers keep it busy.
 //               Each warp's commits track only its own MMAs.
 //   warps 3-10  epilogue: warp w reads TMEM lanes 32*(w%4).. and column half
-//               (w-3)/4, 128 FP32 accumulators per thread; a finished tile
+//               (w-3)/4, 128 FP32 accumulators per thread (64 in the split-K
+//               flavour); a finished tile
 //               is converted to BF16 into the warp's 8 KB staging buffer and
 //               written by TMA tensor stores (plain stores for ragged rows).
-//   TMEM: two 256-column partial buffers (all 512 columns), so the MMA of
-//   k-block kb+1 overlaps the promotion of kb.
-// Decode-sized problems (fewer output tiles than half the SMs) run the
-// split-K flavour: a cluster of 2-4 CTAs per tile, each over a slice of the
-// k-blocks.  Each CTA stages its FP32 partial tile in its own (by then idle)
+//   TMEM: two partial buffers as wide as the tile (all 512 columns for the
+//   256-wide tile), so the MMA of k-block kb+1 overlaps the promotion of kb.
+// Decode-sized problems (fewer 256-wide output tiles than half the SMs) run
+// the split-K flavour: 128-wide tiles, so that twice as many CTAs share the
+// work and each k-block's MMA and promotion take half as long, and a cluster
+// of 1-4 CTAs per tile, each over a slice of the k-blocks.  Each CTA stages its FP32 partial tile in its own (by then idle)
 // pipeline buffers; rank r then reads rows [r*128/S, (r+1)*128/S) of all S
 // partials through distributed shared memory, sums them in rank order and
 // stores them (reduce-scatter, no global scratch, deterministic).
@@ -53,24 +55,33 @@
 namespace fp8rl {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128;
-// Pipeline depth: the split-K flavour (decode shapes, DRAM-latency bound)
-// keeps 4 stages; the others keep 3 and spend the freed 48 KB on output
-// staging, so the epilogue never waits for its previous tile's stores.
-constexpr int kMaxStages = 4;
-__host__ __device__ constexpr int stages_of(bool split) { return split ? 4 : 3; }
+constexpr int BM = 128, BK = 128;
 constexpr int kThreads = 352;            // 11 warps
 constexpr int kAStage = BM * BK;                 // 16 KB
-constexpr int kBStage = BN * BK;                 // 32 KB
-constexpr int kStageBytes = kAStage + kBStage;   // 48 KB
 constexpr int kMaxExperts = 1024;
-constexpr uint32_t kTmemCols = 512;
 constexpr int kMGroup = 16;                      // m-tiles per raster band (L2 reuse)
+constexpr int kMaxStages = 6;
 
-// tcgen05 instruction descriptor, kind::f8f6f4: D = F32 (bits 4-5 = 1),
-// A = B = E4M3 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// The two tile flavours.  Wide (dense and grouped): 128 x 256 tiles, 3 stages
+// of 48 KB, and the freed 48 KB spent on output staging so the epilogue never
+// waits for its previous tile's stores.  Split-K (decode shapes): 128 x 128
+// tiles and 6 stages of 32 KB, the same 192 KB, to keep more DRAM reads in
+// flight.
+template <bool kSplit>
+struct Flavour {
+  static constexpr int kBN = kSplit ? 128 : 256;
+  static constexpr int kStages = kSplit ? 6 : 3;
+  static constexpr int kBStage = kBN * BK;
+  static constexpr int kStageBytes = kAStage + kBStage;
+  static constexpr int kHalf = kBN / 2;             // columns per epilogue warp
+  static constexpr uint32_t kTmemCols = 2 * kBN;    // two partial buffers
+  // tcgen05 instruction descriptor, kind::f8f6f4: D = F32 (bits 4-5 = 1),
+  // A = B = E4M3 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0),
+  // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+  static constexpr uint32_t kIdesc =
+      (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+};
+static_assert(Flavour<false>::kStages <= kMaxStages && Flavour<true>::kStages <= kMaxStages, "");
 
 struct SharedTail {
   uint64_t full[kMaxStages];
@@ -94,18 +105,21 @@ constexpr int kYBoxBytes = kYBox * kYBoxCols * 2;
 constexpr int kYWarpBytes = 2 * kYBoxBytes;
 constexpr size_t kTailPad = (sizeof(SharedTail) + 1023) / 1024 * 1024;
 constexpr size_t smem_bytes(bool split) {
-  return 1024 + (size_t)stages_of(split) * kStageBytes + kTailPad + (split ? 0 : 8 * (size_t)kYWarpBytes);
+  return split ? 1024 + (size_t)Flavour<true>::kStages * Flavour<true>::kStageBytes + kTailPad
+               : 1024 + (size_t)Flavour<false>::kStages * Flavour<false>::kStageBytes + kTailPad +
+                     8 * (size_t)kYWarpBytes;
 }
 static_assert(smem_bytes(false) <= 232448 && smem_bytes(true) <= 232448, "shared memory budget");
 
 // Split-K flavour: a cluster owns exactly one tile, so once its last MMA has
 // completed the stage buffers are idle and hold the FP32 partial tile,
-// [128 rows][kRedLd] (row pitch 1040 B: 16-byte stores by consecutive rows
+// [128 rows][kRedLd] (row pitch 528 B: 16-byte stores by consecutive rows
 // and 16-byte loads along a row are both bank-conflict free).
-constexpr int kRedLd = BN + 4;
+constexpr int kRedLd = Flavour<true>::kBN + 4;
 constexpr int kMaxSplit = 4;
 constexpr int kRedBatch = 4;             // row chunks whose loads are in flight together
-static_assert((size_t)BM * kRedLd * sizeof(float) <= (size_t)stages_of(true) * kStageBytes,
+static_assert((size_t)BM * kRedLd * sizeof(float) <=
+                  (size_t)Flavour<true>::kStages * Flavour<true>::kStageBytes,
               "the partial tile must fit in the stage buffers");
 
 struct GemmArgs {
@@ -146,7 +160,7 @@ struct Tile {
   int e;         // expert (0 when dense)
 };
 
-template <bool kGrouped>
+template <bool kGrouped, int kBN>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const SharedTail* st) {
   Tile tl;
   if (!kGrouped) {
@@ -159,7 +173,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const Shar
     const int nt = local / gs;
     tl.m0 = mt * BM;
     tl.row_end = g.M;
-    tl.n0 = nt * BN;
+    tl.n0 = nt * kBN;
     tl.brow = tl.n0;
     tl.e = 0;
   } else {
@@ -176,7 +190,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const Shar
     const int nt = local / mtiles;
     tl.m0 = st->seg[e] + mt * BM;
     tl.row_end = st->seg[e + 1];
-    tl.n0 = nt * BN;
+    tl.n0 = nt * kBN;
     tl.brow = e * g.N + tl.n0;
     tl.e = e;
   }
@@ -243,7 +257,8 @@ __device__ __forceinline__ void reduce_rows(uint32_t red, int crank, int nsplit,
                                             int row_end, int n0, const GemmArgs& g, int et) {
   const int lo = (BM * crank) / nsplit;
   const int hi = min((BM * (crank + 1)) / nsplit, row_end - m0);
-  const int tasks = (hi - lo) * (BN / 4);
+  constexpr int kV = Flavour<true>::kBN / 4;   // 16-byte vectors per row
+  const int tasks = (hi - lo) * kV;
   uint32_t base[kMaxSplit];
 #pragma unroll
   for (int pr = 0; pr < kMaxSplit; ++pr) base[pr] = mapa(red, (uint32_t)(pr < nsplit ? pr : 0));
@@ -252,7 +267,7 @@ __device__ __forceinline__ void reduce_rows(uint32_t red, int crank, int nsplit,
 #pragma unroll
     for (int b = 0; b < kRedBatch; ++b) {
       const int t = t0 + b * kThreads;
-      const int r = lo + t / (BN / 4), c4 = t % (BN / 4);
+      const int r = lo + t / kV, c4 = t % kV;
       const uint32_t off = (uint32_t)((r * kRedLd + c4 * 4) * (int)sizeof(float));
 #pragma unroll
       for (int pr = 0; pr < kMaxSplit; ++pr)
@@ -262,7 +277,7 @@ __device__ __forceinline__ void reduce_rows(uint32_t red, int crank, int nsplit,
     for (int b = 0; b < kRedBatch; ++b) {
       const int t = t0 + b * kThreads;
       if (t >= tasks) break;
-      const int r = lo + t / (BN / 4), c4 = t % (BN / 4);
+      const int r = lo + t / kV, c4 = t % kV;
       float4 v = p[b][0];
 #pragma unroll
       for (int pr = 1; pr < kMaxSplit; ++pr) {
@@ -297,15 +312,17 @@ template <bool kGrouped, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmY, const GemmArgs g) {
-  constexpr int STAGES = stages_of(kSplit);
+  using F = Flavour<kSplit>;
+  constexpr int STAGES = F::kStages;
+  constexpr int kBN = F::kBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * kAStage;
-  SharedTail* st = reinterpret_cast<SharedTail*>(smem + STAGES * kStageBytes);
+  SharedTail* st = reinterpret_cast<SharedTail*>(smem + STAGES * F::kStageBytes);
   float* red = reinterpret_cast<float*>(smem);   // split-K: aliases the idle stage buffers
-  uint8_t* ystage = smem + STAGES * kStageBytes + kTailPad;   // unused by split-K
+  uint8_t* ystage = smem + STAGES * F::kStageBytes + kTailPad;   // unused by split-K
   volatile uint32_t* abort_flag = &st->abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -334,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!kSplit) tma_prefetch_map(&tmY);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&st->tmem_base), kTmemCols);
+    tmem_alloc(smem_u32(&st->tmem_base), F::kTmemCols);
   }
   if (kGrouped) build_expert_schedule(g, st);
   tc_fence_before();
@@ -350,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       bool alive = true;
       for (int t = cid; t < total_tiles && alive; t += ncl) {
-        const Tile tl = decode_tile<kGrouped>(t, g, st);
+        const Tile tl = decode_tile<kGrouped, kBN>(t, g, st);
         for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -359,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t fb = smem_u32(&st->full[s]);
-          mbar_expect_tx(fb, kStageBytes);
+          mbar_expect_tx(fb, F::kStageBytes);
           tma_load_2d(smem_u32(sA + s * kAStage), &tmA, fb, kb * BK, tl.m0);
-          tma_load_2d(smem_u32(sB + s * kBStage), &tmB, fb, kb * BK, tl.brow);
+          tma_load_2d(smem_u32(sB + s * F::kBStage), &tmB, fb, kb * BK, tl.brow);
         }
       }
       if (!alive) {
@@ -395,12 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+          const uint32_t d = tmem_base + (uint32_t)(buf * kBN);
           const uint32_t a0 = smem_u32(sA + s * kAStage);
-          const uint32_t b0 = smem_u32(sB + s * kBStage);
+          const uint32_t b0 = smem_u32(sB + s * F::kBStage);
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk)
-            mma_f8(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc, kk > 0 ? 1u : 0u);
+            mma_f8(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), F::kIdesc,
+                   kk > 0 ? 1u : 0u);
           mma_commit(smem_u32(&st->empty[s]));
           mma_commit(smem_u32(&st->tfull[buf]));
           last = it;
@@ -416,20 +434,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int h = (warp - 3) >> 2;          // column half of the 256-wide tile
+    const int h = (warp - 3) >> 2;          // column half of the tile (F::kHalf columns)
+    constexpr int kAcc = F::kHalf;          // FP32 accumulators per thread
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t kit = 0;
     bool alive = true;
     for (int t = cid; t < total_tiles && alive; t += ncl) {
-      const Tile tl = decode_tile<kGrouped>(t, g, st);
+      const Tile tl = decode_tile<kGrouped, kBN>(t, g, st);
       const int row = tl.m0 + q * 32 + lane;
       const bool row_ok = row < tl.row_end;
-      const int nbi = tl.n0 / 128 + h;
+      // weight block of this column half (both halves of a 128-wide tile share one)
+      const int nbi = tl.n0 / 128 + (kSplit ? 0 : h);
       const float* swp = g.sw + ((int64_t)tl.e * g.NB + nbi) * KB;
       const bool nb_ok = nbi < g.NB;
-      float acc[128];
+      float acc[kAcc];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < kAcc; ++j) acc[j] = 0.0f;
       // scales of the next k-block are loaded one iteration ahead so their
       // latency hides behind the current promotion
       float sa_next = row_ok ? __ldg(g.sa + (int64_t)kb_lo * g.M + row) : 0.0f;
@@ -446,13 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         okw = __all_sync(0xFFFFFFFFu, okw);
         if (!okw) { alive = false; break; }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + h * 128);
+        const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * kBN + h * kAcc);
         uint32_t p[16];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < kAcc / 16; ++c) {
           tmem_ld16(taddr + c * 16, p);
           tmem_wait_ld();
-          if (c == 7) {
+          if (c == kAcc / 16 - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&st->tempty[buf]));
@@ -463,66 +483,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!alive) break;
-      if (kSplit) {
+      if constexpr (kSplit) {
         // The last tfull wait above means every MMA of this CTA has completed:
         // the stage buffers are idle.  Stage this row of the partial there.
-        float* mine = red + (size_t)(q * 32 + lane) * kRedLd + h * 128;
+        float* mine = red + (size_t)(q * 32 + lane) * kRedLd + h * kAcc;
 #pragma unroll
-        for (int j = 0; j < 128; j += 4)
+        for (int j = 0; j < kAcc; j += 4)
           *reinterpret_cast<float4*>(mine + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-        continue;
-      }
-      const int row0 = tl.m0 + q * 32;
-      if (row0 + kYBox <= tl.row_end) {
-        // The warp's 32 rows all belong to this tile: stage them as two
-        // 32 x 64 boxes and write them with TMA tensor stores (the tensor map
-        // clips columns beyond N).  The buffer was last read by the stores of
-        // this warp's previous tile, a whole tile of k-blocks ago.
-        const uint32_t stg = smem_u32(ystage + (warp - 3) * kYWarpBytes);
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float* a8 = acc + c * 64 + j * 8;
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(a8[0], a8[1]);
-            __nv_bfloat162 b1 = __floats2bfloat162_rn(a8[2], a8[3]);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(a8[4], a8[5]);
-            __nv_bfloat162 b3 = __floats2bfloat162_rn(a8[6], a8[7]);
-            // 128-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ (lane & 7)
-            st_shared_v4(stg + (uint32_t)(c * kYBoxBytes + lane * 128 + ((j ^ (lane & 7)) * 16)),
-                         *reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
-                         *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+      } else {
+        const int row0 = tl.m0 + q * 32;
+        if (row0 + kYBox <= tl.row_end) {
+          // The warp's 32 rows all belong to this tile: stage them as two
+          // 32 x 64 boxes and write them with TMA tensor stores (the tensor map
+          // clips columns beyond N).  The buffer was last read by the stores of
+          // this warp's previous tile, a whole tile of k-blocks ago.
+          const uint32_t stg = smem_u32(ystage + (warp - 3) * kYWarpBytes);
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            const int col0 = tl.n0 + h * 128 + c * kYBoxCols;
-            if (col0 < g.N) tma_store_2d(&tmY, stg + (uint32_t)(c * kYBoxBytes), col0, row0);
-          }
-          bulk_commit();
-        }
-      } else if (row_ok) {
-        // ragged rows (the last m-tile, or an expert segment's end): plain stores
-        __nv_bfloat16* yrow = g.y + (int64_t)row * g.ldy;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int col = tl.n0 + h * 128 + c * 8;
-          if (col < g.N) {
-            uint4 v;
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[c * 8 + 0], acc[c * 8 + 1]);
-            __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[c * 8 + 2], acc[c * 8 + 3]);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[c * 8 + 4], acc[c * 8 + 5]);
-            __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[c * 8 + 6], acc[c * 8 + 7]);
-            v.x = *reinterpret_cast<uint32_t*>(&b0);
-            v.y = *reinterpret_cast<uint32_t*>(&b1);
-            v.z = *reinterpret_cast<uint32_t*>(&b2);
-            v.w = *reinterpret_cast<uint32_t*>(&b3);
-            *reinterpret_cast<uint4*>(yrow + col) = v;
+            for (int j = 0; j < 8; ++j) {
+              const float* a8 = acc + c * 64 + j * 8;
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(a8[0], a8[1]);
+              __nv_bfloat162 b1 = __floats2bfloat162_rn(a8[2], a8[3]);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(a8[4], a8[5]);
+              __nv_bfloat162 b3 = __floats2bfloat162_rn(a8[6], a8[7]);
+              // 128-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ (lane & 7)
+              st_shared_v4(stg + (uint32_t)(c * kYBoxBytes + lane * 128 + ((j ^ (lane & 7)) * 16)),
+                           *reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                           *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int col0 = tl.n0 + h * kAcc + c * kYBoxCols;
+              if (col0 < g.N) tma_store_2d(&tmY, stg + (uint32_t)(c * kYBoxBytes), col0, row0);
+            }
+            bulk_commit();
+          }
+        } else if (row_ok) {
+          // ragged rows (the last m-tile, or an expert segment's end): plain stores
+          __nv_bfloat16* yrow = g.y + (int64_t)row * g.ldy;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int col = tl.n0 + h * kAcc + c * 8;
+            if (col < g.N) {
+              uint4 v;
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[c * 8 + 0], acc[c * 8 + 1]);
+              __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[c * 8 + 2], acc[c * 8 + 3]);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[c * 8 + 4], acc[c * 8 + 5]);
+              __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[c * 8 + 6], acc[c * 8 + 7]);
+              v.x = *reinterpret_cast<uint32_t*>(&b0);
+              v.y = *reinterpret_cast<uint32_t*>(&b1);
+              v.z = *reinterpret_cast<uint32_t*>(&b2);
+              v.w = *reinterpret_cast<uint32_t*>(&b3);
+              *reinterpret_cast<uint4*>(yrow + col) = v;
+            }
           }
         }
       }
@@ -535,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (all waits before them are bounded, so every thread gets here).
     cluster_arrive();   // (A) this thread's part of the partial is staged
     cluster_wait();
-    const Tile tl = decode_tile<kGrouped>(cid, g, st);
+    const Tile tl = decode_tile<kGrouped, kBN>(cid, g, st);
     reduce_rows(smem_u32(red), (int)crank, nsplit, tl.m0, tl.row_end, tl.n0, g, tid);
     cluster_arrive();   // (B) this thread reads no peer's shared memory any more
   }
@@ -543,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc(tmem_base, F::kTmemCols);
   }
   if (kSplit) cluster_wait();   // (B): no peer still reads this CTA's shared memory
 }
@@ -610,13 +630,13 @@ int max_active_clusters(const DeviceState* ds, int s) {
   return n;
 }
 
-// Split-K cluster size for a dense launch: only when the output tiles cannot
-// fill half the GPU, the largest S <= 4 (and <= the k-blocks) for which one
-// cluster per tile fits in one wave.
+// Cluster size S of the split-K flavour for `tiles` 128-wide output tiles:
+// the largest S <= 4 (and <= the k-blocks) for which one cluster of S CTAs
+// per tile fits in one wave, else 1.  The flavour runs only when the 256-wide
+// tiles fill at most half of the SMs, so `tiles` never exceeds the SM count
+// and S = 1 always fits.
 int choose_split(const DeviceState* ds, int64_t tiles, int kb) {
-  const int sms = ds->sm_count;
-  if (tiles <= 0 || tiles * 2 > sms) return 1;
-  int s = (int)std::min<int64_t>(kMaxSplit, sms / tiles);
+  int s = (int)std::min<int64_t>(kMaxSplit, ds->sm_count / std::max<int64_t>(tiles, 1));
   for (s = std::min(s, kb); s >= 2; --s)
     if (max_active_clusters(ds, s) >= tiles) return s;
   return 1;
@@ -655,9 +675,15 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   if (m == 0) return ok();
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FP8RL_OK) return st;
+  // Flavour: 256-wide tiles unless they would fill at most half of the SMs;
+  // then the split-K flavour with 128-wide tiles.
+  const int64_t num_m = (m + BM - 1) / BM;
+  const int64_t wide_tiles = num_m * ((n + Flavour<false>::kBN - 1) / Flavour<false>::kBN);
+  const bool split = wide_tiles * 2 <= ds->sm_count;
+  const int bn = split ? Flavour<true>::kBN : Flavour<false>::kBN;
   CUtensorMap tmA, tmB;
   if ((st = make_map(&tmA, qa, (uint64_t)k, (uint64_t)m, BM, "A")) != FP8RL_OK) return st;
-  if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)n, BN, "W")) != FP8RL_OK) return st;
+  if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)n, (uint32_t)bn, "W")) != FP8RL_OK) return st;
   CUtensorMap tmY;
   if ((st = make_out_map(&tmY, y, (uint64_t)n, (uint64_t)m, (uint64_t)ldy)) != FP8RL_OK) return st;
   GemmArgs g;
@@ -669,16 +695,15 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   g.N = (int)n;
   g.KB = (int)(k / BK);
   g.NB = (int)((n + 127) / 128);
-  g.num_m = (int)((m + BM - 1) / BM);
-  g.num_n = (int)((n + BN - 1) / BN);
+  g.num_m = (int)num_m;
+  g.num_n = (int)((n + bn - 1) / bn);
   g.offsets = nullptr;
   g.E = 1;
   g.status = ds->status;
   const int64_t tiles = (int64_t)g.num_m * g.num_n;
   if (tiles > INT32_MAX) return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "too many tiles");
-  if ((st = set_smem_attr<false, true>(ds)) != FP8RL_OK) return st;
-  g.split = choose_split(ds, tiles, g.KB);
-  if (g.split == 1) {
+  if (!split) {
+    g.split = 1;
     if ((st = set_smem_attr<false, false>(ds)) != FP8RL_OK) return st;
     const int grid = (int)std::min<int64_t>(tiles, ds->sm_count);
     gemm_w8a8_kernel<false, false><<<grid, kThreads, smem_bytes(false), stream>>>(tmA, tmB, tmY, g);
@@ -687,7 +712,9 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   }
   // few tiles: exactly one cluster of g.split CTAs per tile (the kernel's
   // reduction reuses the stage buffers, so a cluster never takes a second
-  // tile), split along K
+  // tile), split along K; a cluster of one when no larger one fits
+  if ((st = set_smem_attr<false, true>(ds)) != FP8RL_OK) return st;
+  g.split = choose_split(ds, tiles, g.KB);
   const int clusters = (int)tiles;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(clusters * g.split), 1, 1);
@@ -727,7 +754,8 @@ extern "C" fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, con
   if ((st = set_smem_attr<true, false>(ds)) != FP8RL_OK) return st;
   CUtensorMap tmA, tmB;
   if ((st = make_map(&tmA, qa, (uint64_t)k, (uint64_t)m_total, BM, "A")) != FP8RL_OK) return st;
-  if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)num_experts * n, BN, "W")) != FP8RL_OK)
+  if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)num_experts * n, Flavour<false>::kBN, "W")) !=
+      FP8RL_OK)
     return st;
   CUtensorMap tmY;
   if ((st = make_out_map(&tmY, y, (uint64_t)n, (uint64_t)m_total, (uint64_t)n)) != FP8RL_OK)
@@ -742,7 +770,7 @@ extern "C" fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, con
   g.KB = (int)(k / BK);
   g.NB = (int)(n / 128);
   g.num_m = 0;
-  g.num_n = (int)((n + BN - 1) / BN);
+  g.num_n = (int)((n + Flavour<false>::kBN - 1) / Flavour<false>::kBN);
   g.offsets = offsets;
   g.E = num_experts;
   g.status = ds->status;

@@ -9,6 +9,7 @@ Cases (device footprint in parentheses):
   aquant          1x128 activation quantization, M=8192 K=4096 (0.1 GB)
   gemm_prefill    act-quant'ed W8A8 GEMM, gate_up shape M=8192 N=24576 K=4096 (0.6 GB)
   gemm_decode     W8A8 GEMM, qkv shape M=256 N=6144 K=4096 (0.03 GB)
+  gemm_decode_o   W8A8 GEMM, o shape M=256 N=4096 K=4096 (0.02 GB; split-K clusters of 2)
   grouped         grouped W8A8 GEMM, Qwen3-30B-A3B gate_up, 128 experts (0.5 GB)
   kv              KV calibrate + quantize, 8 x 20480 tokens x 8 x 128 (0.5 GB)
   tis             TIS weights over 64 x 20480 tokens (0.02 GB)
@@ -49,8 +50,9 @@ def main(argv=None):
     elif c == "aquant":
         a = wl.dense_acts(8192, 4096, seed=1, device=dev)
         run = lambda: fp8rl.quantize_act_groupwise(a)  # noqa: E731
-    elif c in ("gemm_prefill", "gemm_decode"):
-        m, n, k = (8192, 24576, 4096) if c == "gemm_prefill" else (256, 6144, 4096)
+    elif c in ("gemm_prefill", "gemm_decode", "gemm_decode_o"):
+        m, n, k = {"gemm_prefill": (8192, 24576, 4096), "gemm_decode": (256, 6144, 4096),
+                   "gemm_decode_o": (256, 4096, 4096)}[c]
         qa, sa = fp8rl.quantize_act_groupwise(wl.dense_acts(m, k, seed=2, device=dev))
         qw, sw = fp8rl.quantize_weights_blockwise(wl.make_weight(n, k, seed=3, device=dev))
         y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)

@@ -57,11 +57,12 @@ def test_tiny_linear():
                                            # several tiles per CTA, ragged last n-tile
                                            (8192, 1392, 256, 8),
                                            (1000, 1280, 640, 16),
-                                           # split-K clusters: S = 3 with uneven row slices
-                                           # and a ragged last m-tile, S = 2, S = 4 with a
-                                           # ragged n-tile and padded rows
+                                           # split-K flavour (128-wide tiles): S = 3 with
+                                           # uneven row slices and a ragged last m-tile,
+                                           # S = 1 (128 tiles), S = 4 with a ragged n-tile
+                                           # and padded rows, S = 2 (decode o-projection)
                                            (200, 768, 384, 0), (500, 4096, 1024, 0),
-                                           (100, 720, 4096, 24)])
+                                           (100, 720, 4096, 24), (256, 4096, 1024, 0)])
 def test_shapes(m, n, k, ldy_pad):
     _full_case(m, n, k, seed=m + n + k, ldy_pad=ldy_pad)
 
