@@ -180,7 +180,7 @@ def test_split_k_matches_unsplit_on_many_tiles():
     y_big = fp8rl.gemm_w8a8_blockwise(qa, sa, qw, sw)                 # 8 x 8 tiles: no split
     qa_s = qa[:128].contiguous()
     sa_s = sa[:, :128].contiguous()
-    y_small = fp8rl.gemm_w8a8_blockwise(qa_s, sa_s, qw, sw)           # 1 x 8 tiles: split
+    y_small = fp8rl.gemm_w8a8_blockwise(qa_s, sa_s, qw, sw)           # 16 narrow tiles, S = 4
     y64, ab = oracle.gemm_w8a8(np_u8(qa_s), sa_s.cpu().numpy(), np_u8(qw), sw.cpu().numpy())
     check_gemm(y_small, y64, ab, "split-K")
     check_gemm(y_big[:128], y64, ab, "one CTA per tile")
