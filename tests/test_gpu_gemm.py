@@ -176,11 +176,11 @@ def test_split_k_matches_unsplit_on_many_tiles():
     part of a larger launch (one CTA per tile): rows of the small problem must
     agree with the big one within 1 BF16 ulp, and both meet the tolerance."""
     dev = device()
-    qa, sa, qw, sw = _quantized(1024, 2048, 1024, seed=23, dev=dev)
-    y_big = fp8rl.gemm_w8a8_blockwise(qa, sa, qw, sw)                 # 8 x 8 tiles: no split
+    qa, sa, qw, sw = _quantized(1024, 2560, 1024, seed=23, dev=dev)
+    y_big = fp8rl.gemm_w8a8_blockwise(qa, sa, qw, sw)                 # 8 x 10 wide tiles: no split
     qa_s = qa[:128].contiguous()
     sa_s = sa[:, :128].contiguous()
-    y_small = fp8rl.gemm_w8a8_blockwise(qa_s, sa_s, qw, sw)           # 16 narrow tiles, S = 4
+    y_small = fp8rl.gemm_w8a8_blockwise(qa_s, sa_s, qw, sw)           # 20 narrow tiles, S = 4
     y64, ab = oracle.gemm_w8a8(np_u8(qa_s), sa_s.cpu().numpy(), np_u8(qw), sw.cpu().numpy())
     check_gemm(y_small, y64, ab, "split-K")
     check_gemm(y_big[:128], y64, ab, "one CTA per tile")
