@@ -350,6 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&tmB);
     if (!kSplit) tma_prefetch_map(&tmY);
   }
+  // The launch allows programmatic serialization: the launch itself and the
+  // set-up above (barriers, tensor-map prefetch) may overlap the tail of the
+  // previous kernel in the stream.  Nothing touches global memory, and TMEM
+  // is not allocated (a kernel still running on this SM may need it), before
+  // that kernel has completed.
+  grid_dependency_wait();
   if (warp == 1) {
     tmem_alloc(smem_u32(&st->tmem_base), F::kTmemCols);
   }
@@ -642,6 +648,34 @@ int choose_split(const DeviceState* ds, int64_t tiles, int kb) {
   return 1;
 }
 
+// Launches the kernel with programmatic stream serialization allowed (its
+// prologue may overlap the previous kernel; see grid_dependency_wait) and,
+// for the split-K flavour, a cluster of `cluster` CTAs along x.
+template <bool kGrouped, bool kSplit>
+fp8rl_status launch_gemm(int grid, int cluster, cudaStream_t stream, const CUtensorMap& tmA,
+                         const CUtensorMap& tmB, const CUtensorMap& tmY, const GemmArgs& g,
+                         const char* what) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes(kSplit);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (kSplit) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_w8a8_kernel<kGrouped, kSplit>, tmA, tmB, tmY, g),
+                    what);
+}
+
 fp8rl_status check_common(const uint8_t* qa, const float* sa, const uint8_t* qw, const float* sw,
                           int64_t n, int64_t k, const void* y) {
   if (!qa || !sa || !qw || !sw || !y) return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
@@ -706,8 +740,7 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
     g.split = 1;
     if ((st = set_smem_attr<false, false>(ds)) != FP8RL_OK) return st;
     const int grid = (int)std::min<int64_t>(tiles, ds->sm_count);
-    gemm_w8a8_kernel<false, false><<<grid, kThreads, smem_bytes(false), stream>>>(tmA, tmB, tmY, g);
-    st = cuda_check(cudaGetLastError(), "gemm_w8a8_kernel launch");
+    st = launch_gemm<false, false>(grid, 1, stream, tmA, tmB, tmY, g, "gemm_w8a8_kernel launch");
     return st == FP8RL_OK ? ok() : st;
   }
   // few tiles: exactly one cluster of g.split CTAs per tile (the kernel's
@@ -716,20 +749,8 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   if ((st = set_smem_attr<false, true>(ds)) != FP8RL_OK) return st;
   g.split = choose_split(ds, tiles, g.KB);
   const int clusters = (int)tiles;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(clusters * g.split), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(true);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)g.split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  st = cuda_check(cudaLaunchKernelEx(&cfg, gemm_w8a8_kernel<false, true>, tmA, tmB, tmY, g),
-                  "split-K gemm_w8a8_kernel launch");
+  st = launch_gemm<false, true>(clusters * g.split, g.split, stream, tmA, tmB, tmY, g,
+                                "split-K gemm_w8a8_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }
 
@@ -777,7 +798,6 @@ extern "C" fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, con
   const int64_t bound = ((m_total + BM - 1) / BM + num_experts) * (int64_t)g.num_n;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(bound, ds->sm_count));
   g.split = 1;
-  gemm_w8a8_kernel<true, false><<<grid, kThreads, smem_bytes(false), stream>>>(tmA, tmB, tmY, g);
-  st = cuda_check(cudaGetLastError(), "grouped gemm_w8a8_kernel launch");
+  st = launch_gemm<true, false>(grid, 1, stream, tmA, tmB, tmY, g, "grouped gemm_w8a8_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }

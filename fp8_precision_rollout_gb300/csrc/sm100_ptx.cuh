@@ -114,6 +114,13 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch: wait until the grid this one was launched
+// behind has completed and its memory operations are visible.  A no-op when
+// the launch did not allow programmatic serialization.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------- clusters / DSMEM ------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
