@@ -13,6 +13,8 @@ Cases (device footprint in parentheses):
   grouped         grouped W8A8 GEMM, Qwen3-30B-A3B gate_up, 128 experts (0.5 GB)
   kv              KV calibrate + quantize, 8 x 20480 tokens x 8 x 128 (0.5 GB)
   tis             TIS weights over 64 x 20480 tokens (0.02 GB)
+  is_stats        MIS weights + mismatch statistics + weighted token loss, 64 x 20480 tokens
+                  (0.02 GB)
   attention       FP8-KV decode attention, 64 seqs x 4096 tokens, 32 q / 8 KV heads (0.6 GB;
                   one CTA per sequence and KV head, as at 64 x 20480)
   glue_gather     MoE gather + quantize: 4096 tokens x 2048 -> 32768 routed rows (0.1 GB)
@@ -74,6 +76,13 @@ def main(argv=None):
     elif c == "tis":
         lt, lr = wl.tis_logprobs(64 * 20480, seed=5, device=dev, kind="student_t")
         run = lambda: fp8rl.tis_weights(lt, lr)  # noqa: E731
+    elif c == "is_stats":
+        lt, lr = wl.tis_logprobs(64 * 20480, seed=5, device=dev, kind="student_t")
+        loss = torch.randn(lt.numel(), generator=torch.Generator().manual_seed(8)).to(dev)
+        w = torch.empty(lt.numel(), dtype=torch.float32, device=dev)
+        stats = torch.empty(6, dtype=torch.float64, device=dev)
+        run = lambda: fp8rl.is_weights_stats(lt, lr, None, 2.0, 0.5, fp8rl.FP8RL_IS_MASK,  # noqa: E731
+                                             w=w, stats=stats, loss=loss)
     elif c == "attention":
         k = wl.kv_tensor(seed=6, device=dev, seqs=64, tokens=4096)
         kq, ks = fp8rl.quantize_kv_fp8(k, fp8rl.FP8RL_KV_CALIBRATE)
