@@ -10,7 +10,9 @@ per step, no fast-math, no FMA contraction); this module marshals numpy arrays
 into it and adds the few steps that are clearer in Python:
 
 * the exact resolution of the rare TIS inputs whose binary32 rounding the
-  float64 ``exp`` cannot decide (a 60-digit ``decimal`` exponential), and
+  float64 ``exp`` cannot decide (a 60-digit ``decimal`` exponential), and of
+  the rare MoE-glue products silu(g) * u that lie too close to a BF16
+  rounding midpoint for float64 (80-digit ``decimal``),
 * the clip / mask of the TIS weights (numpy ``where``), and
 * the BF16 rounding of float64 GEMM outputs (a torch CPU cast).
 
@@ -68,9 +70,11 @@ def lib():
                                                     P, i64, P, P, ctypes.c_int]
         L.orc_tis_exp.restype = i64
         L.orc_tis_exp.argtypes = [P, P, i64, P, P, i64, ctypes.c_int]
-        L.orc_glue_exp32.argtypes = [P, P, i64, ctypes.c_int]
         L.orc_float_to_bf16.argtypes = [P, P, i64]
-        L.orc_silu_mul_bf16.argtypes = [P, i64, i64, i64, P, ctypes.c_int]
+        L.orc_silu_mul_pairs.restype = i64
+        L.orc_silu_mul_pairs.argtypes = [P, P, i64, P, P, i64, ctypes.c_int]
+        L.orc_silu_mul_bf16.restype = i64
+        L.orc_silu_mul_bf16.argtypes = [P, i64, i64, i64, P, P, i64, ctypes.c_int]
         _LIB = L
     return _LIB
 
@@ -160,14 +164,6 @@ def quantize_act_gather(a, rows):
     return quantize_act_groupwise(torch.from_numpy(np.ascontiguousarray(ab[idx])).view(torch.bfloat16))
 
 
-def glue_exp32(x) -> np.ndarray:
-    """The MoE glue's binary32 exponential (see glue_exp32 in fp8rl_oracle.cpp)."""
-    xf = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
-    out = np.empty_like(xf)
-    lib().orc_glue_exp32(_p(xf), _p(out), xf.size, threads())
-    return out
-
-
 def float_to_bf16(x) -> np.ndarray:
     """binary32 -> BF16 bits, round to nearest even."""
     xf = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
@@ -176,18 +172,109 @@ def float_to_bf16(x) -> np.ndarray:
     return out
 
 
+def _bf16_value(bits: int) -> Decimal:
+    """Exact value of a finite BF16 bit pattern; +-inf stands for +-2^128 (the
+    point past which round-to-nearest overflows)."""
+    mag = bits & 0x7FFF
+    if mag == 0x7F80:
+        v = Decimal(2 ** 128)                          # exact integer
+    else:
+        v = Decimal(float(np.array([mag << 16], dtype=np.uint32).view(np.float32)[0]))
+    return v.copy_negate() if bits & 0x8000 else v    # exact (no context rounding)
+
+
+def silu_mul_decimal(gb: int, ub: int, guess: int) -> int:
+    """BF16_RNE(silu(g) * u) decided in 80-digit decimal arithmetic, for the
+    finite non-zero g and u whose float64 product lies too close to a BF16
+    rounding midpoint.  `guess` is the float64 result; the exact one is it or
+    a neighbour in magnitude.  silu(g) = g / (1 + e^-g) for g > 0 and
+    g e^g / (1 + e^g) for g < 0 (the same function).  If e^-g underflows even
+    the decimal exponent range (g > ~2e18), the decimal value is g * u itself
+    while the true product is strictly smaller in magnitude: a tie is then
+    broken towards zero, and any other tie is an error (the product of a
+    non-zero BF16 and silu(g) is never exactly a midpoint)."""
+    from decimal import MAX_EMAX, MIN_EMIN
+    g = _bf16_value(gb)
+    u = _bf16_value(ub)
+    with localcontext() as ctx:
+        ctx.prec = 80
+        ctx.Emin = MIN_EMIN
+        ctx.Emax = MAX_EMAX
+        if g > 0:
+            s = g / (1 + (-g).exp())
+        else:
+            e = g.exp()
+            s = g * e / (1 + e)
+        x = s * u
+        sign = guess & 0x8000
+        cands = {guess}
+        mag = guess & 0x7FFF
+        if mag < 0x7F80:
+            cands.add(sign | (mag + 1))
+        if mag > 0:
+            cands.add(sign | (mag - 1))
+        dist = sorted((abs(_bf16_value(c) - x), c) for c in cands)
+        if dist[0][0] == dist[1][0]:
+            if g > 0 and s == g:            # e^-g underflowed: |silu(g) u| < |g u|
+                return min(dist[0][1], dist[1][1], key=lambda c: c & 0x7FFF)
+            raise AssertionError("exact BF16 tie for g=%r u=%r" % (g, u))
+        return dist[0][1]
+
+
+def _resolve_hard(gbits: np.ndarray, ubits: np.ndarray, y: np.ndarray, hard: np.ndarray):
+    for i in hard:
+        y.flat[i] = silu_mul_decimal(int(gbits.flat[i]), int(ubits.flat[i]), int(y.flat[i]))
+
+
+def silu_mul_pairs(g_bits, u_bits) -> np.ndarray:
+    """Elementwise BF16_RNE(silu(g) * u) for BF16 bit patterns (uint16 arrays of
+    one shape); see silu_mul_bf16 for the definition."""
+    g = np.ascontiguousarray(np.asarray(g_bits, dtype=np.uint16))
+    u = np.ascontiguousarray(np.broadcast_to(np.asarray(u_bits, dtype=np.uint16), g.shape))
+    y = np.empty(g.shape, dtype=np.uint16)
+    cap = max(4096, g.size // 256)
+    hard = np.empty(cap, dtype=np.int64)
+    cnt = lib().orc_silu_mul_pairs(_p(g), _p(u), g.size, _p(y), _p(hard), cap, threads())
+    if cnt > cap:
+        hard = np.empty(cnt, dtype=np.int64)
+        cnt = lib().orc_silu_mul_pairs(_p(g), _p(u), g.size, _p(y), _p(hard), cnt, threads())
+    _resolve_hard(g, u, y, hard[:cnt])
+    silu_mul_pairs.last_hard_count = int(cnt)
+    return y
+
+
+silu_mul_pairs.last_hard_count = 0
+
+
 def silu_mul_bf16(h):
     """MoE glue between the expert GEMMs: h BF16 [m, 2*inter] = [gate | up]
-    (the gate_up projection's output), y = BF16(silu(gate) * up), BF16 [m, inter].
-    silu(g) = g / (1 + e^-g) with the glue exponential; every step one binary32
-    operation, BF16 rounding to nearest even at the end."""
+    (the gate_up projection's output), y BF16 [m, inter].
+
+    Definition (the pages fix no activation arithmetic; summary page, section
+    3.4.1 names the expert layers fc1/fc2 as quantized): y = BF16_RNE(silu(g) * u)
+    with silu(g) = g / (1 + e^-g), the real product rounded once to the
+    nearest BF16 (ties to even).  Special values as the IEEE evaluation of
+    g * sigma(g) * u: NaN in -> NaN, silu(+inf) = +inf, silu(-inf) = NaN,
+    silu(+-0) = +-0, 0 * inf = NaN.  Computed in float64, with the rare
+    products near a rounding midpoint decided in decimal."""
     import torch
     hb = _u16(h)
     m, two_i = hb.shape
     inter = two_i // 2
     y = np.empty((m, inter), dtype=np.uint16)
-    lib().orc_silu_mul_bf16(_p(hb), m, inter, two_i, _p(y), threads())
+    cap = max(4096, y.size // 256)
+    hard = np.empty(cap, dtype=np.int64)
+    cnt = lib().orc_silu_mul_bf16(_p(hb), m, inter, two_i, _p(y), _p(hard), cap, threads())
+    if cnt > cap:
+        hard = np.empty(cnt, dtype=np.int64)
+        cnt = lib().orc_silu_mul_bf16(_p(hb), m, inter, two_i, _p(y), _p(hard), cnt, threads())
+    _resolve_hard(np.ascontiguousarray(hb[:, :inter]), np.ascontiguousarray(hb[:, inter:]), y,
+                  hard[:cnt])
+    silu_mul_bf16.last_hard_count = int(cnt)
     return torch.from_numpy(y.view(np.int16)).view(torch.bfloat16)
+
+
+silu_mul_bf16.last_hard_count = 0
 
 
 def silu_mul_quantize(h):
@@ -278,7 +365,7 @@ def bf16_round(y64) -> np.ndarray:
 
 # --------------------------------------------------------------------- TIS --
 
-_F32_OVERFLOW = Decimal(2) ** 128   # RN overflows to inf at/after the midpoint below this
+_F32_OVERFLOW = Decimal(2 ** 128)   # exact; RN overflows to inf at/after the midpoint below this
 
 
 def _dec(f32: np.float32) -> Decimal:

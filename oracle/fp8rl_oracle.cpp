@@ -129,38 +129,72 @@ float scale_from_amax(float amax) { return amax / 448.0f; }
 
 // ------------------------------------------------------- MoE glue (SiLU) --
 
-// Reading for the MoE SiLU glue (the pages fix no activation arithmetic): the
-// exponential is this algorithm, one IEEE binary32 operation per step, which
-// the GPU restates step for step:
-//   x > 88 -> +inf, x < -86 -> 0 (1 + e^x rounds to 1 there), NaN -> NaN;
-//   k = rint(fl32(x * RN(log2 e)));
-//   r = fma(-k, RN(ln2), x); r = fma(-k, RN(ln2 - RN(ln2)), r)   (Cody-Waite);
-//   p = degree-7 Taylor polynomial of e^r (coefficients RN(1/n!)), Horner
-//       with fma, ending ... fma(p, r, 1), fma(p, r, 1);
-//   e = p * 2^k (an exact product: |k| <= 127, result normal).
-float glue_exp32(float x) {
-  if (x != x) return x;
-  if (x > 88.0f) return INFINITY;
-  if (x < -86.0f) return 0.0f;
-  const float kf = std::rint(x * 0x1.715476p+0f);
-  float r = std::fma(-kf, 0x1.62e43p-1f, x);
-  r = std::fma(-kf, -0x1.05c61p-29f, r);
-  float p = 0x1.a01a02p-13f;            // 1/7!
-  p = std::fma(p, r, 0x1.6c16c2p-10f);  // 1/6!
-  p = std::fma(p, r, 0x1.111112p-7f);   // 1/5!
-  p = std::fma(p, r, 0x1.555556p-5f);   // 1/4!
-  p = std::fma(p, r, 0x1.555556p-3f);   // 1/3!
-  p = std::fma(p, r, 0.5f);
-  p = std::fma(p, r, 1.0f);
-  p = std::fma(p, r, 1.0f);
-  return p * std::ldexp(1.0f, (int)kf);
+// The MoE glue between the expert GEMMs (summary page, section 3.4.1 names
+// the expert layers fc1/fc2 among the quantized linears; the pages fix no
+// activation arithmetic).  Reading: the gated activation of the Qwen3 family,
+//   y = BF16_RNE( silu(g) * u ),   silu(g) = g / (1 + e^-g),
+// the real-number product rounded ONCE to the nearest BF16 value (ties to
+// even, overflow to +-inf, underflow to a subnormal or a signed zero).  For
+// finite non-zero g, silu(g) is transcendental (Lindemann), so the product is
+// never exactly a rounding midpoint.  Special values follow the IEEE
+// evaluation of g * sigma(g) * u: a NaN input gives NaN; silu(+inf) = +inf;
+// silu(-inf) = -inf * 0 = NaN; silu(+-0) = +-0; then +-0 * inf = NaN, a
+// non-zero finite silu times +-inf is +-inf, and times +-0 is a signed zero.
+//
+// Here the product is formed in float64 (relative error below 2^-50) and
+// rounded to BF16 exactly from that value.  Inputs whose float64 value lies
+// within 2^-40 (relative) of a BF16 rounding midpoint are reported to the
+// caller, which decides them in 80-digit decimal arithmetic.
+
+const uint16_t kBf16QuietNaN = 0x7FC0;
+
+// Nearest BF16 (bit pattern) to the finite float64 x, ties to even; sets
+// *hard when x is within 2^-40 (relative) of a rounding midpoint.
+uint16_t bf16_nearest(double x, bool* hard) {
+  const uint16_t sign = std::signbit(x) ? 0x8000 : 0x0000;
+  const double a = std::fabs(x);
+  if (a == 0.0) return sign;
+  if (a >= std::ldexp(1.0, 128)) return sign | 0x7F80;
+  int ex;
+  std::frexp(a, &ex);
+  const int e = ex - 1;                        // a in [2^e, 2^(e+1))
+  const int qe = (e < -126 ? -126 : e) - 7;    // spacing of BF16 values around a
+  const double t = std::ldexp(a, -qe);         // exact: a in units of the spacing
+  double n = std::floor(t);
+  const double frac = t - n;                   // exact
+  if (std::fabs(frac - 0.5) <= std::ldexp(t, -40)) *hard = true;
+  if (frac > 0.5 || (frac == 0.5 && std::fmod(n, 2.0) != 0.0)) n += 1.0;
+  const double v = std::ldexp(n, qe);          // a BF16 value (or 2^128)
+  if (v >= std::ldexp(1.0, 128)) return sign | 0x7F80;
+  const float f = (float)v;                    // exact
+  uint32_t b;
+  std::memcpy(&b, &f, 4);
+  return (uint16_t)(sign | (b >> 16));
 }
 
-// silu(g) * u = (g / (1 + e^-g)) * u, each step one binary32 operation.
-float glue_silu_mul(float g, float u) {
-  const float den = 1.0f + glue_exp32(-g);
-  const float s = g / den;
-  return s * u;
+// y = BF16_RNE(silu(g) * u) for BF16 inputs (bit patterns).
+uint16_t silu_mul_bf16_one(uint16_t gb, uint16_t ub, bool* hard) {
+  const double g = bf16_to_float(gb), u = bf16_to_float(ub);
+  if (std::isnan(g) || std::isnan(u)) return kBf16QuietNaN;
+  const uint16_t sx = (std::signbit(g) != std::signbit(u)) ? 0x8000 : 0x0000;
+  if (std::isinf(g)) {
+    if (g < 0 || u == 0.0) return kBf16QuietNaN;
+    return (uint16_t)(sx | 0x7F80);
+  }
+  if (g == 0.0) return std::isinf(u) ? kBf16QuietNaN : sx;
+  // g finite and non-zero: silu(g) is non-zero with the sign of g
+  if (std::isinf(u)) return (uint16_t)(sx | 0x7F80);
+  if (u == 0.0) return sx;
+  double s;
+  if (g > 0) {
+    s = g / (1.0 + std::exp(-g));
+  } else {
+    const double e = std::exp(g);              // 0 below about -745: |y| rounds to 0 there
+    s = g * e / (1.0 + e);
+  }
+  const double x = s * u;
+  if (x == 0.0) return sx;                     // |x| < 2^-900: far below the smallest BF16
+  return bf16_nearest(x, hard);
 }
 
 // binary32 -> BF16, round to nearest even (NaN stays a quiet NaN).
@@ -171,6 +205,21 @@ uint16_t float_to_bf16(float f) {
   b += 0x7FFFu + ((b >> 16) & 1u);
   return (uint16_t)(b >> 16);
 }
+
+// Collects the indices of flagged inputs from a parallel loop.
+struct HardList {
+  std::vector<std::vector<int64_t>> per_thread;
+  explicit HardList(int threads) : per_thread((size_t)std::max(threads, 1)) {}
+  int64_t emit(int64_t* out, int64_t max_out) const {
+    int64_t cnt = 0;
+    for (auto& v : per_thread)
+      for (int64_t i : v) {
+        if (cnt < max_out) out[cnt] = i;
+        ++cnt;
+      }
+    return cnt;
+  }
+};
 
 extern "C" {
 
@@ -424,27 +473,52 @@ int64_t orc_tis_exp(const float* lt, const float* lr, int64_t n, float* e32,
   return cnt;
 }
 
-void orc_glue_exp32(const float* x, float* out, int64_t n, int threads) {
-  parallel_for(n, threads, [&](int64_t lo, int64_t hi) {
-    for (int64_t i = lo; i < hi; ++i) out[i] = glue_exp32(x[i]);
-  });
-}
-
 void orc_float_to_bf16(const float* x, uint16_t* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = float_to_bf16(x[i]);
 }
 
+// y[i] = BF16_RNE(silu(g[i]) * u[i]) over n pairs of BF16 bit patterns.
+// Indices whose rounding the float64 value cannot decide go to `hard`;
+// returns how many there are (all are counted, at most max_hard written).
+int64_t orc_silu_mul_pairs(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* y,
+                           int64_t* hard, int64_t max_hard, int threads) {
+  HardList found(threads);
+  const int64_t nthreads = std::max(threads, 1);
+  const int64_t chunk = (n + nthreads - 1) / nthreads;
+  parallel_for(nthreads, threads, [&](int64_t tlo, int64_t thi) {
+    for (int64_t t = tlo; t < thi; ++t) {
+      const int64_t i0 = t * chunk, i1 = std::min(n, i0 + chunk);
+      for (int64_t i = i0; i < i1; ++i) {
+        bool h = false;
+        y[i] = silu_mul_bf16_one(g[i], u[i], &h);
+        if (h) found.per_thread[t].push_back(i);
+      }
+    }
+  });
+  return found.emit(hard, max_hard);
+}
+
 // Gated activation of one MoE expert layer: h is BF16 [m, 2*inter] (row
 // stride ldh) holding gate (columns [0, inter)) then up ([inter, 2*inter));
-// y = BF16(silu(gate) * up), BF16 [m, inter].
-void orc_silu_mul_bf16(const uint16_t* h, int64_t m, int64_t inter, int64_t ldh, uint16_t* y,
-                       int threads) {
-  parallel_for(m, threads, [&](int64_t lo, int64_t hi) {
-    for (int64_t r = lo; r < hi; ++r)
-      for (int64_t c = 0; c < inter; ++c)
-        y[r * inter + c] = float_to_bf16(
-            glue_silu_mul(bf16_to_float(h[r * ldh + c]), bf16_to_float(h[r * ldh + inter + c])));
+// y = BF16_RNE(silu(gate) * up), BF16 [m, inter] dense.  Flagged elements
+// (flat index r * inter + c) go to `hard` as in orc_silu_mul_pairs.
+int64_t orc_silu_mul_bf16(const uint16_t* h, int64_t m, int64_t inter, int64_t ldh, uint16_t* y,
+                          int64_t* hard, int64_t max_hard, int threads) {
+  HardList found(threads);
+  const int64_t nthreads = std::max(threads, 1);
+  const int64_t chunk = (m + nthreads - 1) / nthreads;
+  parallel_for(nthreads, threads, [&](int64_t tlo, int64_t thi) {
+    for (int64_t t = tlo; t < thi; ++t) {
+      const int64_t r0 = t * chunk, r1 = std::min(m, r0 + chunk);
+      for (int64_t r = r0; r < r1; ++r)
+        for (int64_t c = 0; c < inter; ++c) {
+          bool hd = false;
+          y[r * inter + c] = silu_mul_bf16_one(h[r * ldh + c], h[r * ldh + inter + c], &hd);
+          if (hd) found.per_thread[t].push_back(r * inter + c);
+        }
+    }
   });
+  return found.emit(hard, max_hard);
 }
 
 }  // extern "C"
