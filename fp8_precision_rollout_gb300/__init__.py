@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     decode_attention_fp8kv,
     device_status,
     gemm_w8a8_blockwise,
+    inject_device_status,
     grouped_gemm_w8a8_blockwise,
     is_weights_stats,
     is_weights_stats_loss,
@@ -24,6 +25,8 @@ from .binding import (  # noqa: F401
     quantize_weights_blockwise,
     quantize_weights_blockwise_multi,
     quantize_weights_blockwise_multi_host,
+    selftest_bounded_wait,
+    silu_mul_bf16,
     silu_mul_quantize,
     tis_weights,
     version,

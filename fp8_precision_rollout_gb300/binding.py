@@ -73,9 +73,12 @@ def load(path: Optional[str] = None):
         "fp8rl_quantize_weights_blockwise_multi_host": (ctypes.c_int, [P, i32, P, ctypes.c_size_t,
                                                                        P]),
         "fp8rl_silu_mul_quantize": (ctypes.c_int, [P, i64, i64, i64, P, P, P]),
+        "fp8rl_silu_mul_bf16": (ctypes.c_int, [P, i64, i64, i64, P, i64, P]),
         "fp8rl_decode_attention_fp8kv": (ctypes.c_int, [P, P, P, P, P, P, P, i32, i32, i32, i32,
                                                         i32, i32, i32, f32, P, P]),
         "fp8rl_device_status": (ctypes.c_int, [i32, i32]),
+        "fp8rl_inject_device_status": (ctypes.c_int, [i32, ctypes.c_uint32, ctypes.c_uint32]),
+        "fp8rl_selftest_bounded_wait": (ctypes.c_int, [i32, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -303,6 +306,22 @@ def silu_mul_quantize(h, q: Optional[torch.Tensor] = None, scales: Optional[torc
     return q, scales
 
 
+def silu_mul_bf16(h, y: Optional[torch.Tensor] = None, stream=None):
+    """h = [gate | up] BF16 [m, 2*inter] -> y = BF16_RNE(silu(gate) * up), BF16 [m, inter]."""
+    _dev(h, torch.bfloat16, "h")
+    _rowmajor(h, "h")
+    m, two_i = h.shape
+    if two_i % 2:
+        raise ValueError("h must have an even number of columns (gate | up)")
+    inter = two_i // 2
+    if y is None:
+        y = torch.empty(m, inter, dtype=torch.bfloat16, device=h.device)
+    _rowmajor(_dev(y, torch.bfloat16, "y"), "y")
+    _check(load().fp8rl_silu_mul_bf16(h.data_ptr(), m, inter, h.stride(0), y.data_ptr(),
+                                      y.stride(0), _stream(stream)))
+    return y
+
+
 # -------------------------------------------------------------- attention --
 
 def decode_attention_fp8kv(q, k_cache, v_cache, k_scale, v_scale, seq_lens, block_table=None,
@@ -450,3 +469,13 @@ def device_status(device: int = 0, clear: bool = True) -> int:
     st = load().fp8rl_device_status(device, 1 if clear else 0)
     _check(st)
     return st
+
+
+def inject_device_status(device: int, flags: int, site: int = 0):
+    """Overwrite the device status word (error-path tests; see fp8rl.h)."""
+    _check(load().fp8rl_inject_device_status(device, flags, site))
+
+
+def selftest_bounded_wait(limit_us: int, stream=None):
+    """Launch the bounded-wait self-test kernel (its wait times out; see fp8rl.h)."""
+    _check(load().fp8rl_selftest_bounded_wait(int(limit_us), _stream(stream)))

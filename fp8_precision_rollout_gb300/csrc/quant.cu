@@ -3,8 +3,8 @@
 //   * per-token 1x128-group activation quantization (FP8-RL summary, sections
 //     3.4.1/3.4.2 Phase 3, dynamic quantization), plain and gathering the
 //     routed rows of an MoE layer,
-//   * the MoE glue SiLU(gate) * up + 1x128 quantization between the expert
-//     GEMMs,
+//   * the MoE glue y = BF16_RNE(SiLU(gate) * up), alone or with the 1x128
+//     quantization of y, between the expert GEMMs,
 //   * FP8 E4M3 KV-cache quantization with per-head scales, given or
 //     calibrated from the tensor (section 3.4.4).
 //
@@ -83,63 +83,175 @@ __global__ void __launch_bounds__(256) aquant_kernel(const uint16_t* __restrict_
 }
 
 // ------------------------------------------------------------- MoE glue --
+//
+// y = BF16_RNE(silu(g) * u), silu(g) = g / (1 + e^-g): the real product rounded
+// once to the nearest BF16 (declared in fp8rl.h).  silu depends on the BF16
+// gate alone, so each device holds it for all 65536 gate patterns as an
+// unevaluated float-float pair hi + lo (relative error near 2^-48), formed in
+// double precision once, when the library first meets the device.  The
+// product hi*u + lo*u carries an exact FMA error term, and the BF16 rounding
+// of that float-float value is decided from the binary32 product's bits, so
+// y is the correctly rounded product unless it lies within about 2^-46 of a
+// rounding midpoint (none does: the GPU tests compare every gate with every
+// up mantissa and exponent against the oracle).
+//
+// Entries by the gate's exponent field eg and sign ("scale" K: the pair
+// holds silu(g) * 2^K):
+//   |g| < 2^-60 (eg < 67):   K = 100;
+//   -128 < g <= -64:          K = 140;   -256 < g <= -128: K = 240;
+//   g <= -256:                hi = 0 (|y| is below half the smallest BF16
+//                             for every finite u);
+//   otherwise:                K = 0 ("natural" entries);
+//   +-0, +-inf, NaN:          unused (special values).
+// Where the remainder silu*2^K - hi underflows binary32, lo is the smallest
+// subnormal with the remainder's sign: products g*u or (g/2)*u that are
+// exactly BF16 midpoints round in that direction.
+// g_silu_pair holds (hi, lo) of every entry; g_silu_hi holds hi for the
+// natural entries and 0 for all others, so the fast path reads 4 bytes and a
+// zero product sends everything else to the general path.
+__device__ float2 g_silu_pair[65536];
+__device__ float g_silu_hi[65536];
 
-// The glue exponential E(x) (declared in fp8rl.h): Cody-Waite reduction by
-// ln2 with FMA, degree-7 Taylor polynomial in Horner form with FMA, exact
-// scaling by 2^k; one binary32 operation per step.
-__device__ __forceinline__ float glue_exp32(float x) {
-  if (x != x) return x;
-  if (x > 88.0f) return __int_as_float(0x7F800000);
-  if (x < -86.0f) return 0.0f;
-  const float kf = rintf(fx::fmul(x, 0x1.715476p+0f));
-  float r = fx::ffma(-kf, 0x1.62e43p-1f, x);
-  r = fx::ffma(-kf, -0x1.05c61p-29f, r);
-  float p = 0x1.a01a02p-13f;
-  p = fx::ffma(p, r, 0x1.6c16c2p-10f);
-  p = fx::ffma(p, r, 0x1.111112p-7f);
-  p = fx::ffma(p, r, 0x1.555556p-5f);
-  p = fx::ffma(p, r, 0x1.555556p-3f);
-  p = fx::ffma(p, r, 0.5f);
-  p = fx::ffma(p, r, 1.0f);
-  p = fx::ffma(p, r, 1.0f);
-  return fx::fmul(p, __int_as_float(((int)kf + 127) << 23));   // |k| <= 127: exact
+__device__ __forceinline__ int silu_scale(uint32_t gb) {
+  const uint32_t eg = (gb >> 7) & 0xFFu;
+  if (eg < 67u) return 100;
+  if ((gb & 0x8000u) && eg == 133u) return 140;
+  if ((gb & 0x8000u) && eg >= 134u) return 240;
+  return 0;
 }
-
-// binary32 -> BF16 bits, round to nearest even (NaN stays a quiet NaN).
-__device__ __forceinline__ uint32_t bf16_rne_bits(float f) {
-  uint32_t b = __float_as_uint(f);
-  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return (b >> 16) | 0x0040u;
-  b += 0x7FFFu + ((b >> 16) & 1u);
-  return b >> 16;
-}
-
-// silu(g) = fl32(g / fl32(1 + E(-g))) for every BF16 gate g, indexed by its
-// 16 bits.  The glue's activation depends on the gate alone, so it is formed
-// once per device (init_glue_tables, at the library's first use of the
-// device) with exactly this arithmetic, and the kernel looks it up.
-__device__ float g_silu_tab[65536];
 
 __global__ void silu_table_kernel() {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < 65536) {
-    const float g = __uint_as_float((uint32_t)i << 16);
-    const float den = fx::fadd(1.0f, glue_exp32(-g));
-    g_silu_tab[i] = fx::fdiv(g, den);
+  const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= 65536u) return;
+  const float gf = __uint_as_float(i << 16);
+  const uint32_t eg = (i >> 7) & 0xFFu;
+  float hi = 0.0f, lo = 0.0f;
+  if (eg != 0xFFu && gf != 0.0f && !((i & 0x8000u) && eg >= 135u)) {
+    const double g = (double)gf;
+    const double sc = ldexp(1.0, silu_scale(i));
+    double a, b;          // silu(g) * 2^K = a + b, |b| far below |a|
+    float sticky;         // sign of the remainder if it underflows
+    if (eg < 115u) {      // |g| < 2^-12: g/2 + g^2/4 - g^4/96 (next term below 2^-70 relative)
+      const double g2 = fx::dmul(g, g);
+      a = fx::dmul(fx::dmul(g, 0.5), sc);
+      b = fx::dmul(fx::dsub(fx::dmul(g2, 0.25), fx::ddiv(fx::dmul(g2, g2), 96.0)), sc);
+      sticky = 0x1p-149f;             // silu(g) - g/2 > 0
+    } else if (!(i & 0x8000u)) {      // g >= 2^-12: silu = g - c, c = g e^-g / (1 + e^-g)
+      const double e = exp(-g);
+      a = g;
+      b = -fx::ddiv(fx::dmul(g, e), fx::dadd(1.0, e));
+      sticky = -0x1p-149f;            // silu(g) < g
+    } else {                          // g <= -2^-12: g e^g / (1 + e^g)
+      const double e = exp(g);
+      a = fx::dmul(fx::ddiv(fx::dmul(g, e), fx::dadd(1.0, e)), sc);
+      b = 0.0;
+      sticky = 0.0f;
+    }
+    hi = fx::d2f(fx::dadd(a, b));
+    lo = fx::d2f(fx::dadd(fx::dsub(a, (double)hi), b));
+    if (lo == 0.0f) lo = sticky;
   }
+  g_silu_pair[i] = make_float2(hi, lo);
+  g_silu_hi[i] = silu_scale(i) == 0 ? hi : 0.0f;
+}
+
+// The general path: special values, the scaled entries and products below
+// 2^-100.  Works on magnitudes: |x| = (P + T) 2^(eh + eu - K) with P the
+// binary32 product of the two significands in [1, 4) and T its exact error
+// plus the table's lo term; rounds to the BF16 spacing at |x| (subnormal
+// spacing 2^-133 below 2^-126).
+__device__ __noinline__ uint32_t silu_mul_bf16_general(uint32_t gb, uint32_t ub) {
+  const float2 t = g_silu_pair[gb];
+  const float hs = t.x, ls = t.y;
+  const uint32_t sx = (gb ^ ub) & 0x8000u;
+  const uint32_t ag = gb & 0x7FFFu, au = ub & 0x7FFFu;
+  if (ag > 0x7F80u || au > 0x7F80u) return 0x7FC0u;          // a NaN input
+  if (ag == 0x7F80u) {                                        // g = +-inf
+    if ((gb & 0x8000u) || au == 0u) return 0x7FC0u;           // silu(-inf) = -inf * 0; inf * 0
+    return (ub & 0x8000u) | 0x7F80u;
+  }
+  if (ag == 0u) return au == 0x7F80u ? 0x7FC0u : sx;          // silu(+-0) = +-0
+  if (au == 0x7F80u) return sx | 0x7F80u;                     // non-zero silu times +-inf
+  if (au == 0u || hs == 0.0f) return sx;                      // a signed zero
+  const int K = silu_scale(gb);
+  const uint32_t hb = __float_as_uint(hs);                    // a normal number
+  const int eh = (int)((hb >> 23) & 0xFFu) - 127;             // in [-121, 54] here
+  const float mh = __uint_as_float((hb & 0x007FFFFFu) | 0x3F800000u);
+  float ln = fx::fmul(fabsf(ls), __uint_as_float((uint32_t)(127 - eh) << 23));
+  if ((__float_as_uint(ls) ^ hb) & 0x80000000u) ln = -ln;     // > 0 increases |x|
+  uint32_t ubits = au << 16;
+  int eu = -127;
+  if ((au >> 7) == 0u) {                                      // subnormal u: scale by 2^64 (exact)
+    ubits = __float_as_uint(fx::fmul(__uint_as_float(ubits), 0x1p64f));
+    eu -= 64;
+  }
+  eu += (int)((ubits >> 23) & 0xFFu);
+  const float mu = __uint_as_float((ubits & 0x007FFFFFu) | 0x3F800000u);
+  const float P = fx::fmul(mh, mu);
+  const float E1 = fx::ffma(mh, mu, -P);                     // exact error of P
+  const float T = E1 == 0.0f ? fx::fmul(ln, mu) : fx::ffma(ln, mu, E1);   // keeps ln's sign
+  const int ep = P >= 2.0f ? 1 : 0;
+  const int E = ep + eh + eu - K;                             // |x| in [2^E, 2^(E+1)) before rounding
+  if (E > 127) return sx | 0x7F80u;
+  int qe = ep - 7;                                            // BF16 spacing in P's units
+  if (E < -126) qe = min(qe - 126 - E, ep + 2);               // subnormal spacing (or all to zero)
+  const float Q = __uint_as_float((uint32_t)(127 + qe) << 23);
+  const float nq = truncf(fx::fmul(P, __uint_as_float((uint32_t)(127 - qe) << 23)));
+  const float f = fx::fsub(P, fx::fmul(nq, Q));               // exact
+  const float d = fx::fadd(fx::fsub(f, fx::fmul(0.5f, Q)), T);
+  const bool up = d != 0.0f ? d > 0.0f : !(__float_as_uint(T) >> 31);
+  const uint32_t n = (uint32_t)nq + (up ? 1u : 0u);
+  uint32_t bits = E >= -126 ? ((uint32_t)(E + 127) << 7) + n - 128u : n;
+  if (bits > 0x7F80u) bits = 0x7F80u;
+  return sx | bits;
+}
+
+// y = BF16_RNE(silu(g) * u) for BF16 bit patterns gb, ub (low 16 bits).
+// Fast path: a natural entry with |hi * u| >= 2^-100 (then hi*u - p is exact).
+__device__ __forceinline__ uint32_t silu_mul_bf16(uint32_t gb, uint32_t ub) {
+  const float hi = __ldg(&g_silu_hi[gb]);
+  const float u = __uint_as_float(ub << 16);
+  const float p = fx::fmul(hi, u);
+  if (fabsf(p) >= 0x1p-100f) {
+    const uint32_t b = __float_as_uint(p);
+    if ((b & 0xFFFFu) - 0x7FFCu <= 8u) {
+      // within 4 binary32 ulps of a BF16 midpoint m: the sign of
+      // (p - m) + (hi*u - p) + lo*u decides.  An exact product leaves a zero
+      // error term; then lo*u alone keeps its sign even when it underflows.
+      const float lo = __ldg(&g_silu_pair[gb].y);
+      const float e = fx::ffma(hi, u, -p);
+      const float c = e == 0.0f ? fx::fmul(lo, u) : fx::ffma(lo, u, e);
+      const float m = __uint_as_float((b & 0xFFFF0000u) | 0x8000u);
+      const float d = fx::fadd(fx::fsub(p, m), c);
+      const uint32_t ds = __float_as_uint(d != 0.0f ? d : c);
+      return (b >> 16) + (((ds ^ b) >> 31) ? 0u : 1u);
+    }
+    return (b + 0x7FFFu + ((b >> 16) & 1u)) >> 16;            // p decides alone
+  }
+  return silu_mul_bf16_general(gb, ub);
 }
 
 // Two BF16 lanes (packed in a 32-bit word) of gate and up -> the packed BF16
 // pair silu(g) * u.
 __device__ __forceinline__ uint32_t silu_mul2(uint32_t g2, uint32_t u2) {
-  uint32_t out = 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t gb = h ? (g2 >> 16) : (g2 & 0xFFFFu);
-    const float u = __uint_as_float((h ? (u2 >> 16) : (u2 & 0xFFFFu)) << 16);
-    const float y = fx::fmul(__ldg(&g_silu_tab[gb]), u);
-    out |= bf16_rne_bits(y) << (16 * h);
+  return silu_mul_bf16(g2 & 0xFFFFu, u2 & 0xFFFFu) | (silu_mul_bf16(g2 >> 16, u2 >> 16) << 16);
+}
+
+// y[r, c] = BF16_RNE(silu(h[r, c]) * h[r, inter + c]); 8 outputs per thread
+// and step (16-byte loads and stores), grid-stride over the row vectors.
+__global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t* __restrict__ h, int64_t inter,
+                                                       int64_t ldh, uint16_t* __restrict__ y,
+                                                       int64_t ldy, int64_t n_vec) {
+  const int64_t vpr = inter / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n_vec; v += stride) {
+    const int64_t r = v / vpr, c = (v - r * vpr) * 8;
+    const uint4 gv = ld_stream(h + r * ldh + c);
+    const uint4 uv = ld_stream(h + r * ldh + inter + c);
+    *reinterpret_cast<uint4*>(y + r * ldy + c) =
+        make_uint4(silu_mul2(gv.x, uv.x), silu_mul2(gv.y, uv.y), silu_mul2(gv.z, uv.z),
+                   silu_mul2(gv.w, uv.w));
   }
-  return out;
 }
 
 // Gated activation + 1x128 quantization: the task layout of aquant_kernel
@@ -346,6 +458,27 @@ extern "C" fp8rl_status fp8rl_silu_mul_quantize(const void* h, int64_t m, int64_
   silu_quant_kernel<<<grid_for(ctas, ds, per_sm), 256, 0, stream>>>(
       reinterpret_cast<const uint16_t*>(h), m, inter, ldh, q, scales, tasks, kb);
   st = cuda_check(cudaGetLastError(), "silu_quant_kernel launch");
+  return st == FP8RL_OK ? ok() : st;
+}
+
+extern "C" fp8rl_status fp8rl_silu_mul_bf16(const void* h, int64_t m, int64_t inter, int64_t ldh,
+                                            void* y, int64_t ldy, cudaStream_t stream) {
+  if (m < 0 || inter < 1 || ldh < 2 * inter || ldy < inter)
+    return fail(FP8RL_ERR_INVALID_ARG, "need m >= 0, inter >= 1, ldh >= 2 * inter, ldy >= inter");
+  if (m == 0) return ok();
+  if (!h || !y) return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (inter % 8 || ldh % 8 || ldy % 8)
+    return fail(FP8RL_ERR_ALIGNMENT, "inter, ldh and ldy must be multiples of 8");
+  if (!aligned(h, 16) || !aligned(y, 16))
+    return fail(FP8RL_ERR_ALIGNMENT, "h and y must be 16-byte aligned");
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  if (st != FP8RL_OK) return st;
+  const int64_t n_vec = m * (inter / 8);
+  static const int per_sm = resident_ctas_per_sm(silu_mul_kernel, 256);
+  silu_mul_kernel<<<grid_for((n_vec + 255) / 256, ds, per_sm), 256, 0, stream>>>(
+      reinterpret_cast<const uint16_t*>(h), inter, ldh, reinterpret_cast<uint16_t*>(y), ldy, n_vec);
+  st = cuda_check(cudaGetLastError(), "silu_mul_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }
 

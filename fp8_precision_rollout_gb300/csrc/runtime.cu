@@ -7,6 +7,7 @@
 #include <string>
 
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace fp8rl {
 
@@ -141,4 +142,64 @@ extern "C" fp8rl_status fp8rl_device_status(int32_t device, int32_t clear) {
   if (words[0] & kStatusBadIndex)
     return fail(FP8RL_ERR_INVALID_ARG, "a device-side row index was out of range (row left zero)");
   return ok();
+}
+
+// ---------------------------------------------------------- error-path tests --
+
+extern "C" fp8rl_status fp8rl_inject_device_status(int32_t device, uint32_t flags, uint32_t site) {
+  if (flags & ~(uint32_t)(kStatusTimeout | kStatusBadIndex))
+    return fail(FP8RL_ERR_INVALID_ARG, "unknown status flags 0x%x", flags);
+  int prev = -1;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return cuda_check(e, "cudaGetDevice");
+  if (device != prev) {
+    e = cudaSetDevice(device);
+    if (e != cudaSuccess) return cuda_check(e, "cudaSetDevice");
+  }
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  if (st == FP8RL_OK) {
+    const uint32_t words[2] = {flags, site};
+    st = cuda_check(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+    if (st == FP8RL_OK)
+      st = cuda_check(cudaMemcpy(ds->status, words, sizeof(words), cudaMemcpyHostToDevice),
+                      "writing the device status word");
+  }
+  if (device != prev) cudaSetDevice(prev);
+  return st == FP8RL_OK ? ok() : st;
+}
+
+namespace fp8rl {
+namespace {
+constexpr uint32_t kSelfTestSite = 90;
+
+// One CTA of one warp: lane 0 waits on an mbarrier that nothing arrives on,
+// through the pipelines' bounded wait with a short limit.  The wait gives up,
+// records the timeout and the site in the status word, and the kernel returns
+// normally; the context stays usable.
+__global__ void bounded_wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    ptx::mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    (void)ptx::mbar_wait(ptx::smem_u32(&bar), 0u, &abort_flag, status, kSelfTestSite, limit_ns);
+  __syncthreads();
+}
+}  // namespace
+}  // namespace fp8rl
+
+extern "C" fp8rl_status fp8rl_selftest_bounded_wait(int32_t limit_us, cudaStream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(FP8RL_ERR_INVALID_ARG, "limit_us must be in [1, 1000000] (got %d)", limit_us);
+  DeviceState* ds = nullptr;
+  fp8rl_status st = device_state(&ds);
+  if (st != FP8RL_OK) return st;
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(ds->status, (uint64_t)limit_us * 1000ull);
+  st = cuda_check(cudaGetLastError(), "bounded_wait_selftest_kernel launch");
+  return st == FP8RL_OK ? ok() : st;
 }

@@ -51,17 +51,18 @@ __device__ __forceinline__ uint64_t gtimer() {
 // Bounded wait for the completion of the phase with parity `parity`.
 // Returns false if the CTA is aborting: this wait ran out of time (then it
 // raises the abort flag and records `site` in the status word), or another
-// role of the CTA already raised the flag.
+// role of the CTA already raised the flag.  `limit_ns` is kWaitLimitNs for
+// every pipeline wait; only the self-test kernel passes a shorter one.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity,
                                           volatile uint32_t* abort_flag, uint32_t* status,
-                                          uint32_t site) {
+                                          uint32_t site, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try(a, parity)) return true;
   const uint64_t t0 = gtimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try(a, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort_flag) return false;
-      if (gtimer() - t0 > kWaitLimitNs) {
+      if (gtimer() - t0 > limit_ns) {
         *abort_flag = 1u;
         atomicOr(status, kStatusTimeout);
         atomicExch(status + 1, site);

@@ -239,21 +239,32 @@ fp8rl_status fp8rl_quantize_act_gather(const void* a, int64_t m_src, int64_t k, 
 
 /* MoE glue between the expert GEMMs: gated activation + quantize.  h holds
  * the gate_up projection's output, gate in columns [0, inter) and up in
- * [inter, 2*inter); y = BF16(silu(gate) * up) is quantized in 1x128 groups
- * as fp8rl_quantize_act_groupwise does (the down projection's input).  The
- * pages fix no activation arithmetic; the reading computed here, one
- * binary32 operation per step: silu(g) = g / (1 + E(-g)), product with u,
- * round to nearest even into BF16, where E is this exponential:
- *   E(x) = +inf for x > 88, 0 for x < -86 (1 + E rounds to 1), NaN for NaN;
- *   k = rint(fl32(x * RN(log2 e))); r = fma(-k, RN(ln2), x);
- *   r = fma(-k, RN(ln2 - RN(ln2)), r); p = Horner with fma over the
- *   binary32 roundings of 1/7!, 1/6!, ..., 1/2!, 1, 1; E = p * 2^k.
+ * [inter, 2*inter); y = BF16_RNE(silu(gate) * up) is quantized in 1x128
+ * groups as fp8rl_quantize_act_groupwise does (the down projection's input).
+ * The pages fix no activation arithmetic (section 3.4.1 names the expert
+ * layers fc1/fc2 among the quantized linears); y is the plain definition,
+ * the real product silu(g) * u with silu(g) = g / (1 + e^-g), rounded once
+ * to the nearest BF16 (ties to even, overflow to +-inf, underflow to a
+ * subnormal or a signed zero).  Special values follow the IEEE evaluation
+ * of g * sigma(g) * u: a NaN input gives NaN, silu(+inf) = +inf,
+ * silu(-inf) = NaN, silu(+-0) = +-0, and 0 * inf = NaN.  Bit-identical to
+ * that definition (fp8rl_silu_mul_bf16 returns y itself).
  *   h        BF16 [m, 2*inter], row stride ldh (>= 2*inter); inter, ldh
  *            multiples of 8; 16-byte aligned
  *   q        E4M3 [m, inter] (row stride inter), 8-byte aligned
  *   scales   FP32 [ceil(inter/128), m] group-major */
 fp8rl_status fp8rl_silu_mul_quantize(const void* h, int64_t m, int64_t inter, int64_t ldh,
                                      uint8_t* q, float* scales, cudaStream_t stream);
+
+/* The gated activation of fp8rl_silu_mul_quantize without the quantization:
+ * y[r, c] = BF16_RNE(silu(h[r, c]) * h[r, inter + c]) (same definition and
+ * special values), for a BF16 down projection or for inspecting y.
+ *   h        BF16 [m, 2*inter], row stride ldh (>= 2*inter)
+ *   y        BF16 [m, inter], row stride ldy (>= inter)
+ * Requires inter, ldh, ldy multiples of 8 and h, y 16-byte aligned; m = 0
+ * is a no-op. */
+fp8rl_status fp8rl_silu_mul_bf16(const void* h, int64_t m, int64_t inter, int64_t ldh, void* y,
+                                 int64_t ldy, cudaStream_t stream);
 
 /* Decode attention over an FP8 E4M3 KV cache (section 3.4.4: K and V are
  * stored in E4M3 with per-head scales recalibrated every step; the decode
@@ -340,6 +351,23 @@ fp8rl_status fp8rl_is_weights_stats_loss(const float* logp_train, const float* l
  * FP8RL_OK otherwise; clears the word when clear != 0.  device = CUDA
  * ordinal. */
 fp8rl_status fp8rl_device_status(int32_t device, int32_t clear);
+
+/* Error-path support (no counterpart in the pages): lets a caller's tests
+ * exercise its handling of fp8rl_device_status without faulting a GPU.
+ * fp8rl_inject_device_status synchronizes `device` and overwrites its status
+ * word with `flags` (a combination of 1 = wait timeout, 2 = out-of-range
+ * device index; anything else is FP8RL_ERR_INVALID_ARG) and `site` (reported
+ * in the timeout message).  Not stream-ordered; do not call it while a
+ * capture is in progress. */
+fp8rl_status fp8rl_inject_device_status(int32_t device, uint32_t flags, uint32_t site);
+
+/* Launches on `stream` one small kernel that waits on a device-side barrier
+ * nothing will complete, through the same bounded wait the pipelined kernels
+ * use but with a limit of `limit_us` microseconds (1 .. 1000000).  The wait
+ * gives up, sets the timeout flag with site 90 in the status word and the
+ * kernel returns; the next fp8rl_device_status reports FP8RL_ERR_TIMEOUT and
+ * the CUDA context stays usable. */
+fp8rl_status fp8rl_selftest_bounded_wait(int32_t limit_us, cudaStream_t stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

@@ -17,9 +17,18 @@ def lib():
     return binding.load()
 
 
+def _exported_fp8rl_symbols():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    return sorted(set(re.findall(r"\b(fp8rl_[a-z0-9_]+)\b", out)))
+
+
 def test_exports_every_declared_symbol(lib):
     declared = binding.declared_symbols()
-    assert len(declared) == 17
+    assert len(declared) >= 18
+    # the library's exported C symbols are exactly the header's declarations
+    assert _exported_fp8rl_symbols() == declared
     for name in declared:
         assert hasattr(lib, name), name
     # and the binding wraps each of them under the same name
@@ -95,3 +104,10 @@ def test_product_path_does_not_import_the_oracle():
                 text = open(os.path.join(root, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "fp8rl_oracle" not in text, f
+
+
+def test_error_path_entries_check_their_arguments_on_the_host(lib):
+    assert lib.fp8rl_inject_device_status(0, 4, 0) == 1            # unknown flag
+    assert "unknown status flags" in binding.last_error()
+    assert lib.fp8rl_selftest_bounded_wait(0, None) == 1            # limit out of range
+    assert lib.fp8rl_selftest_bounded_wait(1000001, None) == 1

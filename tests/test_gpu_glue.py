@@ -2,7 +2,11 @@
 1x128 quantization of expert-sorted rows, and the SiLU(gate) * up +
 quantization between the expert GEMMs, on the Qwen3-30B-A3B routing at full
 size, ragged shapes, strided inputs, special values, and out-of-range
-gather indices (reported, not faulted)."""
+gather indices (reported, not faulted).  The gated activation itself,
+y = BF16_RNE(silu(g) * u), is compared over every BF16 gate with every up
+significand (both signs) and with every up exponent: the rounding of the
+product depends only on the two significands except where it overflows or
+turns subnormal, which the exponent sweep covers."""
 import numpy as np
 import pytest
 import torch
@@ -132,3 +136,71 @@ def test_silu_every_bf16_gate():
                torch.full((512, 128), -1e-3)):
         h = torch.cat([g, up.to(torch.bfloat16)], dim=1)
         _silu_case(h, dev)
+
+
+def _pairs_case(dev, g_bits: np.ndarray, u_rows: np.ndarray):
+    """One row per up value: h[r] = [all gates | u_rows[r] repeated]; y from the
+    library's BF16 entry against the oracle's pairs, bit for bit."""
+    rows, inter = u_rows.size, g_bits.size
+    h = np.empty((rows, 2 * inter), dtype=np.uint16)
+    h[:, :inter] = g_bits[None, :]
+    h[:, inter:] = u_rows[:, None]
+    ht = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev)
+    yc = Canary(rows * inter, torch.bfloat16, dev)
+    y = fp8rl.silu_mul_bf16(ht, yc.view.view(rows, inter))
+    torch.cuda.synchronize()
+    yc.check()
+    got = y.cpu().view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    want = oracle.silu_mul_pairs(np.tile(g_bits, rows), np.repeat(u_rows, inter))
+    bad = got != want
+    if bad.any():
+        i = np.flatnonzero(bad)[:5]
+        raise AssertionError("y differs: g=%s u=%s gpu=%s oracle=%s" % (
+            [hex(x) for x in np.tile(g_bits, rows)[i]], [hex(x) for x in np.repeat(u_rows, inter)[i]],
+            [hex(x) for x in got[i]], [hex(x) for x in want[i]]))
+
+
+def test_silu_mul_bf16_every_gate_every_up_significand():
+    """All 65536 gates x all 256 up significands of [1, 2), both signs (2^25 products)."""
+    dev = device()
+    g = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    for sign in (0x0000, 0x8000):
+        _pairs_case(dev, g, (sign | 0x3F80 | np.arange(128)).astype(np.uint16))
+        _pairs_case(dev, g, (sign | 0x4000 | np.arange(128)).astype(np.uint16))   # [2, 4): odd exponent
+
+
+def test_silu_mul_bf16_every_gate_every_up_exponent():
+    """All gates x every up exponent field (zeros, subnormals, infinities and
+    NaNs included) with three significands and both signs: overflow to inf,
+    subnormal and zero results, and the special values."""
+    dev = device()
+    g = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    for mant in (0x00, 0x5B, 0x7F):
+        for sign in (0x0000, 0x8000):
+            _pairs_case(dev, g, (sign | (np.arange(256) << 7) | mant).astype(np.uint16))
+
+
+def test_silu_mul_bf16_strided_and_random():
+    dev = device()
+    rng = np.random.default_rng(21)
+    m, inter = 37, 392
+    h = rng.integers(0, 1 << 16, size=(m, 2 * inter + 24)).astype(np.uint16)
+    ht = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev)[:, :2 * inter]
+    ybig = torch.zeros(m, inter + 40, dtype=torch.bfloat16, device=dev)
+    fp8rl.silu_mul_bf16(ht, ybig[:, :inter])
+    torch.cuda.synchronize()
+    got = ybig.cpu().view(torch.int16).numpy().view(np.uint16)
+    want = oracle.silu_mul_bf16(torch.from_numpy(np.ascontiguousarray(h[:, :2 * inter]).view(np.int16))
+                                .view(torch.bfloat16)).view(torch.int16).numpy().view(np.uint16)
+    assert (got[:, :inter] == want).all()
+    assert (got[:, inter:] == 0).all()
+
+
+def test_silu_quantize_equals_quantized_bf16_glue():
+    """The fused glue equals the BF16 glue followed by the activation quantizer."""
+    dev = device()
+    h = workloads.expert_inputs(300, 2 * 768, seed=22).to(dev)
+    q1, s1 = fp8rl.silu_mul_quantize(h)
+    q2, s2 = fp8rl.quantize_act_groupwise(fp8rl.silu_mul_bf16(h))
+    torch.cuda.synchronize()
+    assert torch.equal(q1, q2) and torch.equal(s1.view(torch.int32), s2.view(torch.int32))

@@ -5,13 +5,18 @@ re-quantization, activation quantization, dense GEMMs of both flavours,
 gather, grouped GEMM, SiLU glue, KV calibrate and quantize, decode attention,
 TIS, IS statistics with the weighted loss) are run eagerly, then captured and
 replayed into separate outputs; the results must agree bit for bit, except
-the statistics sums, whose FP64 atomic order may differ (counts stay exact)."""
+the statistics sums, whose FP64 atomic order may differ (counts stay exact).
+The replayed outputs are also checked against the oracle directly: codes,
+scales and weights bit for bit, the GEMMs and the attention within their
+tolerances."""
+import numpy as np
 import pytest
 import torch
 
 import fp8_precision_rollout_gb300 as fp8rl
+import oracle
 from fp8_precision_rollout_gb300 import workloads
-from gpu_helpers import device
+from gpu_helpers import check_gemm, device, np_f32_bits, np_u8
 
 pytestmark = pytest.mark.gpu
 
@@ -120,3 +125,65 @@ def test_step_replays_from_a_cuda_graph():
                 assert torch.allclose(x, y, rtol=1e-6, atol=1e-9), key
             else:
                 assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), key
+
+
+def _check_against_oracle(inp, o):
+    for w, q, sc in zip(inp["ws"], o["wq"], o["wsc"]):
+        oq, os_ = oracle.quantize_weights_blockwise(w.cpu())
+        assert (np_u8(q) == oq).all() and (np_f32_bits(sc) == os_.view(np.uint32)).all()
+    for a, key in ((inp["a_pre"], "ap"), (inp["a_dec"], "ad")):
+        oq, os_ = oracle.quantize_act_groupwise(a.cpu())
+        assert (np_u8(o[key + "_q"]) == oq).all()
+        assert (np_f32_bits(o[key + "_s"]) == os_.view(np.uint32)).all()
+    w0q, w0s = np_u8(o["wq"][0]), o["wsc"][0].cpu().numpy()
+    rows = np.arange(0, 1280, 7)
+    y64, ab = oracle.gemm_w8a8(np_u8(o["ap_q"]), o["ap_s"].cpu().numpy(), w0q, w0s, rows=rows)
+    check_gemm(o["y_pre"][torch.from_numpy(rows).to(o["y_pre"].device)], y64, ab, "graph prefill")
+    y64, ab = oracle.gemm_w8a8(np_u8(o["ad_q"]), o["ad_s"].cpu().numpy(), w0q, w0s)
+    check_gemm(o["y_dec"], y64, ab, "graph decode")
+    oq, os_ = oracle.quantize_act_gather(inp["tok"].cpu(), inp["rows"].cpu().numpy())
+    assert (np_u8(o["g_q"]) == oq).all() and (np_f32_bits(o["g_s"]) == os_.view(np.uint32)).all()
+    oq, os_ = oracle.silu_mul_quantize(o["h"].cpu())
+    assert (np_u8(o["s_q"]) == oq).all() and (np_f32_bits(o["s_s"]) == os_.view(np.uint32)).all()
+    kv = inp["kv"].view(-1, 2, 128).cpu()
+    os_ = oracle.kv_calibrate(kv)
+    assert (np_f32_bits(o["ks"]) == os_.view(np.uint32)).all()
+    assert (np_u8(o["kq"]).reshape(-1, 2, 128) == oracle.kv_quantize(kv, os_)).all()
+    ow = oracle.tis_weights(inp["lt"].cpu().numpy(), inp["lr"].cpu().numpy())
+    assert (np_f32_bits(o["tw"]) == ow.view(np.uint32)).all()
+    mw, st, ta = oracle.is_weights_stats(inp["lt"].cpu().numpy(), inp["lr"].cpu().numpy(), None,
+                                         2.0, 0.5, oracle.IS_MASK, inp["loss"].cpu().numpy())
+    assert (np_f32_bits(o["mw"]) == mw.view(np.uint32)).all()
+    got = o["st"].cpu().numpy()
+    assert got[0] == st[0] and got[4] == st[4]
+    assert (np.abs(got - st) <= 2.0 ** -20 * ta + 1e-300).all()
+    kq = np_u8(o["kq"]).reshape(3, 700, 2, 128)
+    o64, mag = oracle.decode_attention_fp8kv(inp["q"].cpu(), kq, kq, o["ks"].cpu().numpy(),
+                                             o["ks"].cpu().numpy(), [700, 1, 333])
+    ag = o["att"].float().cpu().numpy().astype(np.float64)
+    assert (np.abs(ag - o64) <= 2.0 ** -8 * np.abs(o64) + 1e-3 * mag + 1e-30).all()
+
+
+def test_graph_replay_matches_the_oracle():
+    dev = device()
+    inp = _inputs(dev)
+    warm = _outputs(inp, dev)
+    _step(inp, warm)
+    torch.cuda.synchronize()
+    out = _outputs(inp, dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _step(inp, out)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for t in out.values():
+        for x in (t if isinstance(t, list) else [t]):
+            x.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _step(inp, out)
+    g.replay()
+    torch.cuda.synchronize()
+    fp8rl.device_status(0)
+    _check_against_oracle(inp, out)

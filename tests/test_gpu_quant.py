@@ -248,7 +248,8 @@ def test_kv_long_context_full_size():
 
 def test_host_streaming_requant_matches_device_path():
     """Host BF16 in, host codes and scales out, through a workspace small enough
-    to split tensors across chunks; bit-identical to the device multi-tensor path."""
+    to split tensors across chunks; bit-identical to the device multi-tensor path
+    and to the oracle (this is the call the bench's end-to-end figure uses)."""
     dev = device()
     shapes = [(1000, 512), (128, 136), (300, 2048), (7, 8), (640, 1024)]
     ws = [workloads.make_weight(n, k, seed=70 + i) for i, (n, k) in enumerate(shapes)]
@@ -270,4 +271,7 @@ def test_host_streaming_requant_matches_device_path():
     for i in range(len(ws)):
         assert (hq[i].numpy() == qd[i].cpu().numpy()).all(), i
         assert (hs[i].numpy().view(np.uint32) == sd[i].cpu().numpy().view(np.uint32)).all(), i
+        oq, os_ = oracle.quantize_weights_blockwise(ws[i])
+        assert (hq[i].numpy() == oq).all(), i
+        assert (hs[i].numpy().view(np.uint32) == os_.view(np.uint32)).all(), i
     assert (qbig[:, 2048:].numpy() == 0x5A).all()         # row padding untouched

@@ -4,7 +4,8 @@ fp8rl_quantize_kv_fp8_calibrate_noalloc serves callers that cannot let the
 library allocate device memory (for example an engine that hands almost all
 of the GPU's memory to its own pools up front).  Its results must be
 identical to the ordinary fp8rl_quantize_kv_fp8(..., FP8RL_KV_CALIBRATE, ...)
-call.  Two calls in a row check that the shared scratch array is cleared
+call, and both must equal the oracle's KV calibration and quantization bit
+for bit.  Two calls in a row check that the shared scratch array is cleared
 between calls: the first input has much larger maxima than the second, so
 stale maxima would show up as wrong scales.  This file is collected last.
 """
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from fp8_precision_rollout_gb300 import binding, workloads
 from gpu_helpers import device, np_f32_bits, np_u8
 
@@ -57,6 +59,11 @@ def test_noalloc_matches_calibrate_on_two_calls_in_a_row():
         torch.cuda.synchronize()
         assert (np_f32_bits(s) == np_f32_bits(sr)).all()
         assert (np_u8(q) == np_u8(qr)).all()
+        # and directly against the oracle
+        xr = x.view(-1, heads, hd).cpu()
+        os_ = oracle.kv_calibrate(xr)
+        assert (np_f32_bits(s) == os_.view(np.uint32)).all()
+        assert (np_u8(q).reshape(-1, heads, hd) == oracle.kv_quantize(xr, os_)).all()
 
 
 def test_noalloc_rejects_more_heads_than_its_scratch_holds():
