@@ -125,15 +125,20 @@ def sources_sha256(files=WQ_SOURCES) -> str:
     return h.hexdigest()
 
 
-def _profiled_traffic(elements: int):
+def _profiled_traffic(elements: int, write_bytes: int):
+    """DRAM bytes of one full re-quantization launch: the measured DRAM reads
+    per element of the committed capture times the launch's elements, plus
+    the algorithmic writes (the capture's writes were partly still in L2 when
+    it ended, so its write counter undercounts them).  None when the kernel's
+    sources no longer match the capture."""
     path = os.path.join(ROOT, WQ_PROFILE)
     if not os.path.exists(path):
         return None
     for line in open(path):
         if line.startswith("bench-traffic:"):
             d = json.loads(line[len("bench-traffic:"):])
-            if d.get("sources_sha256") == sources_sha256():
-                return d["dram_bytes_per_element"] * elements
+            if d.get("sources_sha256") == sources_sha256() and "dram_read_bytes_per_element" in d:
+                return d["dram_read_bytes_per_element"] * elements + write_bytes
     return None
 
 
@@ -230,13 +235,15 @@ class Workload:
         torch.cuda.synchronize()
 
     # one step; records an event pair around each row on the current stream
+    # (external events: inside a CUDA graph capture they become timed event
+    # record nodes)
     def step(self, ev=None):
         fp8rl, torch = self.fp8rl, self.torch
         launches = 0
 
         def mark(key):
             if ev is not None:
-                e = torch.cuda.Event(enable_timing=True)
+                e = torch.cuda.Event(enable_timing=True, external=True)
                 e.record()
                 ev.setdefault(key, []).append(e)
 
@@ -288,6 +295,10 @@ def _ms(ev, a, b):
 
 
 def _rows(W, ev, steps, peaks):
+    """Per-row times and roofline fractions.  GEMM fractions use the burst FP8
+    peak (2 x the measured cuBLAS bf16 burst; the step is a fraction of a
+    second, not a seconds-long power-capped run); the sustained-peak fractions
+    sit beside them."""
     hbm = peaks["hbm_gbs"]
     fp8_burst = 2.0 * peaks["bf16_tflops"]
     fp8_sust = 2.0 * peaks["bf16_tflops_sustained"]
@@ -304,13 +315,18 @@ def _rows(W, ev, steps, peaks):
         gbytes = m * k + 4 * m * k / 128 + n * k + 4 * (n / 128) * (k / 128) + 2 * m * n
         qbytes = 2 * m * k + m * k + 4 * m * k / 128
         ai = flops / gbytes
-        attain = min(fp8_sust * 1e12, ai * hbm * 1e9) / 1e12
+        attain = min(fp8_burst * 1e12, ai * hbm * 1e9) / 1e12
+        attain_s = min(fp8_sust * 1e12, ai * hbm * 1e9) / 1e12
         out[key] = {"act_quant_ms": tq, "act_quant_gbs": qbytes / tq / 1e6,
                     "act_quant_frac_hbm": qbytes / tq / 1e6 / hbm,
                     "gemm_ms": tg, "tflops": flops / tg / 1e9,
-                    "frac_fp8_peak": flops / tg / 1e9 / fp8_sust,
+                    "frac_fp8_peak": flops / tg / 1e9 / fp8_burst,
                     "frac_attainable": flops / tg / 1e9 / attain,
-                    "bound": "tensor" if ai * hbm * 1e9 > fp8_sust * 1e12 else "hbm"}
+                    "frac_fp8_peak_sustained": flops / tg / 1e9 / fp8_sust,
+                    "frac_attainable_sustained": flops / tg / 1e9 / attain_s,
+                    "pair_ms": tq + tg,
+                    "pair_vs_byte_bound": (tq + tg) / ((qbytes + gbytes) / hbm / 1e6),
+                    "bound": "tensor" if ai * hbm * 1e9 > fp8_burst * 1e12 else "hbm"}
     for g in W.moe:
         key = "moe_" + g["name"]
         n, k, m = g["n"], g["k"], W.moe_rows
@@ -319,7 +335,8 @@ def _rows(W, ev, steps, peaks):
         flops = 2.0 * m * n * k
         gbytes = m * k + 4 * m * k / 128 + 128 * n * k + 128 * 4 * (n / 128) * (k / 128) + 2 * m * n
         ai = flops / gbytes
-        attain = min(fp8_sust * 1e12, ai * hbm * 1e9) / 1e12
+        attain = min(fp8_burst * 1e12, ai * hbm * 1e9) / 1e12
+        attain_s = min(fp8_sust * 1e12, ai * hbm * 1e9) / 1e12
         # glue bytes: gather reads k and writes k + scales per row; SiLU glue reads 2k
         gl_bytes = (2 * m * k if g["name"] == "gate_up" else 4 * m * k) + m * k + 4 * m * k / 128
         out[key] = {"glue": "gather + quantize" if g["name"] == "gate_up" else
@@ -327,9 +344,11 @@ def _rows(W, ev, steps, peaks):
                     "glue_ms": tq, "glue_gbs": gl_bytes / tq / 1e6,
                     "glue_frac_hbm": gl_bytes / tq / 1e6 / hbm,
                     "gemm_ms": tg, "tflops": flops / tg / 1e9,
-                    "frac_fp8_peak": flops / tg / 1e9 / fp8_sust,
+                    "frac_fp8_peak": flops / tg / 1e9 / fp8_burst,
                     "frac_attainable": flops / tg / 1e9 / attain,
-                    "bound": "tensor" if ai * hbm * 1e9 > fp8_sust * 1e12 else "hbm"}
+                    "frac_fp8_peak_sustained": flops / tg / 1e9 / fp8_sust,
+                    "frac_attainable_sustained": flops / tg / 1e9 / attain_s,
+                    "bound": "tensor" if ai * hbm * 1e9 > fp8_burst * 1e12 else "hbm"}
     t = statistics.mean(_ms(ev, "kv_start", "kv_end"))
     kv_elems = sum(x["x"].numel() for x in W.kv)
     kv_bytes = 5 * kv_elems            # calibrate pass reads 2 B, quantize reads 2 + writes 1
@@ -373,6 +392,147 @@ def _cpu_baseline(seconds_target: float = 15.0):
             "kind": "oracle",
             "sample": "Qwen3-8B layer-0 qkv/o/gate_up/down re-quantization (%d elements) x %d" % (
                 sum(w.numel() for w in ws), reps)}
+
+
+def _timed(fn):
+    t0 = time.perf_counter()
+    out = fn()
+    return (time.perf_counter() - t0) * 1e3, out
+
+
+def _cpu_baseline_rows(W):
+    """The oracle timed on every row of the step, on the host cores, with inputs
+    of the same recipes generated on the host.  Full workloads where the
+    oracle finishes in about a second (activation quantization, MoE glue,
+    TIS, MIS); otherwise a sample, scaled to the row's full workload by its
+    work (elements, rows or sequences) and marked "extrapolated".  Returns
+    {row: {"cpu_ms": ms for the row's full workload, "sample": ...,
+    "extrapolated": bool}}."""
+    import numpy as np
+    import torch
+    import oracle
+    from fp8_precision_rollout_gb300 import workloads as wl
+    oracle.lib()
+    out = {}
+    # a1: layer-0 linears, scaled to the 144 tensors by element count
+    ws = [wl.make_weight(n, k, seed=wl.sub_seed(2, 0, i)) for i, (_, n, k) in
+          enumerate(wl.QWEN3_8B_LINEARS)]
+    ms = sum(_timed(lambda w=w: oracle.quantize_weights_blockwise(w))[0] for w in ws)
+    el = sum(w.numel() for w in ws)
+    out["a1_requant"] = {"cpu_ms": ms * W.req_elems / el, "extrapolated": True,
+                         "sample": "layer-0 qkv/o/gate_up/down (%d elements)" % el}
+    # a2 + a3: full activation quantization; GEMMs on one row per host thread
+    # (the oracle parallelizes over rows) x all N
+    nr = max(2, oracle.threads())
+    wq = {}
+    for i, (name, n, k) in enumerate(wl.QWEN3_8B_LINEARS):
+        wq[name] = oracle.quantize_weights_blockwise(ws[i])
+    for g in W.gemms:
+        key = "gemm_%s_m%d" % (g["name"], g["m"])
+        m, n, k = g["m"], g["n"], g["k"]
+        a = wl.dense_acts(m, k, seed=wl.sub_seed(3, m, n, k))
+        tq, (qa, sa) = _timed(lambda: oracle.quantize_act_groupwise(a))
+        rows = (np.arange(nr) * (m // nr)).astype(np.int64)
+        tg, _ = _timed(lambda: oracle.gemm_w8a8(qa, sa, wq[g["name"]][0], wq[g["name"]][1], rows=rows))
+        out[key] = {"act_quant_cpu_ms": tq, "gemm_cpu_ms": tg * m / nr, "extrapolated": True,
+                    "sample": "act-quant: full [%d, %d]; GEMM: %d rows x %d columns, scaled by "
+                              "M/%d" % (m, k, nr, n, nr)}
+    # MoE chain: full glue; grouped GEMMs on 16 rows of one expert x all N
+    offsets, token_of_row, _ = wl.moe_routing(seed=0)
+    toks = wl.dense_acts(wl.MOE_TOKENS, wl.MOE_HIDDEN, seed=wl.sub_seed(5, 1))
+    tgath, (gq, gs) = _timed(lambda: oracle.quantize_act_gather(toks, token_of_row.numpy()))
+    h = wl.expert_inputs(W.moe_rows, 2 * wl.MOE_INTER, seed=11)
+    tsilu, (sq, ss) = _timed(lambda: oracle.silu_mul_quantize(h))
+    for g, (qa, sa), tglue in ((W.moe[0], (gq, gs), tgath), (W.moe[1], (sq, ss), tsilu)):
+        n, k = g["n"], g["k"]
+        wexp = wl.moe_weights(n, k, 1, seed=wl.sub_seed(4, n, k))
+        qw, sw = oracle.quantize_weights_blockwise(wexp.view(-1, k))
+        off1 = np.array([0, nr], dtype=np.int32)
+        tg, _ = _timed(lambda: oracle.grouped_gemm_w8a8(
+            np.ascontiguousarray(qa[:nr]), np.ascontiguousarray(sa[:, :nr]), qw.reshape(1, n, k),
+            sw.reshape(1, n // 128, k // 128), off1))
+        out["moe_" + g["name"]] = {"glue_cpu_ms": tglue, "gemm_cpu_ms": tg * W.moe_rows / nr,
+                                   "extrapolated": True,
+                                   "sample": "glue: full %d rows; grouped GEMM: %d rows of one "
+                                             "expert x %d columns, scaled by rows/%d" % (
+                                                 W.moe_rows, nr, n, nr)}
+    # a5: one sequence of K and V, scaled to 64 sequences
+    tkv = 0.0
+    for t in range(2):
+        x = wl.kv_tensor(seed=wl.sub_seed(6, t), seqs=1).view(-1, 8, 128)
+        dt, s = _timed(lambda: oracle.kv_calibrate(x))
+        dq, _ = _timed(lambda: oracle.kv_quantize(x, s))
+        tkv += dt + dq
+    out["a5_kv"] = {"cpu_ms": tkv * 64, "extrapolated": True,
+                    "sample": "K and V of 1 of 64 sequences (20480 tokens), scaled by 64"}
+    # decode attention: one sequence of the cache, scaled to 64
+    kq = oracle.kv_quantize(x, s).reshape(1, 20480, 8, 128)
+    qh = W.attn_q[:1].cpu()
+    ta, _ = _timed(lambda: oracle.decode_attention_fp8kv(qh, kq, kq, s, s, [20480]))
+    out["a5b_decode_attention"] = {"cpu_ms": ta * 64, "extrapolated": True,
+                                   "sample": "1 of 64 sequences (32 query heads), scaled by 64"}
+    lt, lr = wl.tis_logprobs(64 * 20480, seed=5, kind="student_t")
+    ltn, lrn = lt.numpy(), lr.numpy()
+    tt, _ = _timed(lambda: oracle.tis_weights(ltn, lrn))
+    out["a6_tis"] = {"cpu_ms": tt, "extrapolated": False, "sample": "full (1,310,720 tokens)"}
+    loss = torch.randn(lt.numel(), generator=torch.Generator().manual_seed(8)).numpy()
+    tm, _ = _timed(lambda: oracle.is_weights_stats(ltn, lrn, None, 2.0, 0.5, oracle.IS_MASK, loss))
+    out["a6b_mis_stats"] = {"cpu_ms": tm, "extrapolated": False, "sample": "full (1,310,720 tokens)"}
+    return out
+
+
+def _merge_cpu_rows(rows, cpu):
+    """Adds each row's oracle time and the GPU/oracle speed ratio."""
+    for key, c in cpu.items():
+        r = rows.get(key)
+        if r is None:
+            continue
+        if "cpu_ms" in c:
+            gpu_ms = r.get("ms")
+        else:
+            gpu_ms = (r.get("act_quant_ms", r.get("glue_ms", 0.0)) + r["gemm_ms"])
+            c = dict(c, cpu_ms=c.get("act_quant_cpu_ms", c.get("glue_cpu_ms", 0.0)) + c["gemm_cpu_ms"])
+        r["cpu_baseline"] = dict(c, cores=_cores(), kind="oracle")
+        if gpu_ms:
+            r["cpu_baseline"]["gpu_speedup"] = c["cpu_ms"] / gpu_ms
+
+
+def _cores():
+    import oracle
+    return oracle.threads()
+
+
+def _link_rates(dev, nbytes: int = 1 << 31):
+    """This box's pinned host<->device copy rates (GB/s, best of 3): one
+    direction at a time, and both at once on two streams."""
+    import torch
+    host_a = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    host_b = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dev_a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dev_b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def best(fn):
+        out = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            out.append(time.perf_counter() - t0)
+        return min(out)
+
+    def both():
+        with torch.cuda.stream(s1):
+            dev_a.copy_(host_a, non_blocking=True)
+        with torch.cuda.stream(s2):
+            host_b.copy_(dev_b, non_blocking=True)
+
+    h2d = nbytes / best(lambda: dev_a.copy_(host_a, non_blocking=True)) / 1e9
+    d2h = nbytes / best(lambda: host_b.copy_(dev_b, non_blocking=True)) / 1e9
+    bi = 2 * nbytes / best(both) / 1e9
+    del host_a, host_b, dev_a, dev_b
+    return {"h2d_gbs": h2d, "d2h_gbs": d2h, "bidirectional_gbs": bi, "buffer_bytes": nbytes}
 
 
 def run_reference(args):
@@ -433,13 +593,34 @@ def run_ours(args):
     ev = {}
     sampler = ClockSampler(local)
     launches = 0
+    graph = None
+    if not args.eager:
+        # The timed steps are captured once as a CUDA graph (as a serving
+        # engine captures its step) and replayed: one untimed replay, then the
+        # timed one.  Every kernel and event of the K steps is a graph node.
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            W.step()                                 # warm-up on the capture stream
+        torch.cuda.current_stream().wait_stream(cap)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(args.steps):
+                launches += W.step(ev)
+        graph.replay()
+        torch.cuda.synchronize()
+        fp8rl.device_status(local)
     with sampler:
         barrier()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record()
-        for _ in range(args.steps):
-            launches += W.step(ev)
+        if graph is not None:
+            graph.replay()
+        else:
+            for _ in range(args.steps):
+                launches += W.step(ev)
         t_end.record()
         barrier()
     fp8rl.device_status(local)
@@ -484,11 +665,21 @@ def run_ours(args):
         e2e = {"value": replica_gbs(world, W.req_bytes, e_steps, e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
         del hw, hq, hs, work
+        # the host link's own bound for this step's copies
+        link = _link_rates(dev)
+        t_bound = max(h2d / link["h2d_gbs"], d2h / link["d2h_gbs"],
+                      (h2d + d2h) / link["bidirectional_gbs"]) / 1e9
+        e2e["link"] = link
+        e2e["link_bound"] = W.req_bytes / t_bound / 1e9
+        e2e["frac_of_link_bound"] = e2e["value"] / world / e2e["link_bound"]
 
     # the dominant kernel of the step and its roofline
     a1 = rows["a1_requant"]
     dom = {"bound": "hbm", "achieved": a1["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-           "frac": a1["gbs"] / peaks["hbm_gbs"], "traffic": _profiled_traffic(W.req_elems),
+           "frac": a1["gbs"] / peaks["hbm_gbs"],
+           "traffic": _profiled_traffic(W.req_elems, W.req_elems + 4 * W.req_blocks),
+           "traffic_method": "ncu DRAM reads per element of the layer-0 capture x the launch's "
+                             "elements + algorithmic writes (codes + scales)",
            "kernel": "wquant_kernel (a1 re-quantization)",
            "peak_source": peaks["source"] + " hbm_gbs (copy)"}
     if rank == 0:
@@ -501,12 +692,15 @@ def run_ours(args):
                 "config": {"workload": WORKLOAD,
                            "step": "timed inside the full hot-path step (GEMMs, MoE chain, KV, "
                                    "decode attention, TIS, MIS)",
+                           "launch": ("eager launches" if args.eager else
+                                      "the K timed steps replayed as one CUDA graph"),
                            "parallelism": "replicas" if world > 1 else "single",
                            "l2": "inputs larger than L2: each step streams ~35 GB"},
                 "roofline": dom, "rows": rows, "gpu_launches": launches,
                 "clocks": clocks, "e2e": e2e}
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = _cpu_baseline()
+            _merge_cpu_rows(rows, _cpu_baseline_rows(W))
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -521,6 +715,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the timed steps one by one instead of as a CUDA graph")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
