@@ -193,7 +193,12 @@ class Workload:
                 sa = torch.empty(k // 128, m, dtype=torch.float32, device=dev)
                 y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
                 self.gemms.append(dict(name=name, m=m, n=n, k=k, a=a, qa=qa, sa=sa, y=y,
-                                       qw=self.q[j], sw=self.s[j]))
+                                       qw=self.q[j], sw=self.s[j], fused=(m <= 256)))
+        # decode-sized rows run the fused quantize + stream-K GEMM; one
+        # workspace serves them all (the calls are ordered on one stream)
+        self.dec_ws = torch.zeros(max(fp8rl.linear_w8a8_decode_workspace_bytes(n)
+                                      for _, n, _ in wl.QWEN3_8B_LINEARS),
+                                  dtype=torch.uint8, device=dev)
         # a4 + MoE glue: token matrix -> gather + quantize -> grouped gate_up ->
         # SiLU(gate) * up + quantize -> grouped down
         offsets, token_of_row, counts = wl.moe_routing(seed=0)
@@ -254,6 +259,12 @@ class Workload:
         for g in self.gemms:
             key = "gemm_%s_m%d" % (g["name"], g["m"])
             mark(key + "_start")
+            if g["fused"]:
+                fp8rl.linear_w8a8_decode(g["a"], g["qw"], g["sw"], g["y"], g["qa"], g["sa"],
+                                         self.dec_ws)
+                mark(key + "_end")
+                launches += 1
+                continue
             fp8rl.quantize_act_groupwise(g["a"], g["qa"], g["sa"])
             mark(key + "_mid")
             fp8rl.gemm_w8a8_blockwise(g["qa"], g["sa"], g["qw"], g["sw"], g["y"])
@@ -290,6 +301,37 @@ class Workload:
         return launches
 
 
+def _decode_paths(W, rows, reps: int = 20):
+    """The M = 256 rows two ways, each launched `reps` times back to back
+    outside the step (CUDA events around the loop): the fused one-launch path
+    of the step, and the earlier two-launch path (activation quantizer, then
+    the dense kernel's split-K flavour)."""
+    torch, fp8rl = W.torch, W.fp8rl
+    for g in W.gemms:
+        if not g["fused"]:
+            continue
+        key = "gemm_%s_m%d" % (g["name"], g["m"])
+
+        def fused():
+            fp8rl.linear_w8a8_decode(g["a"], g["qw"], g["sw"], g["y"], g["qa"], g["sa"], W.dec_ws)
+
+        def unfused():
+            fp8rl.quantize_act_groupwise(g["a"], g["qa"], g["sa"])
+            fp8rl.gemm_w8a8_blockwise(g["qa"], g["sa"], g["qw"], g["sw"], g["y"])
+
+        for name, fn in (("fused_back_to_back_ms", fused), ("two_launch_back_to_back_ms", unfused)):
+            fn()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            rows[key][name] = e0.elapsed_time(e1) / reps
+
+
 def _ms(ev, a, b):
     return [x.elapsed_time(y) for x, y in zip(ev[a], ev[b])]
 
@@ -309,6 +351,20 @@ def _rows(W, ev, steps, peaks):
     for g in W.gemms:
         key = "gemm_%s_m%d" % (g["name"], g["m"])
         m, n, k = g["m"], g["n"], g["k"]
+        if g["fused"]:
+            # one launch: act-quant + stream-K GEMM; HBM-bound as a whole
+            t = statistics.mean(_ms(ev, key + "_start", key + "_end"))
+            flops = 2.0 * m * n * k
+            gbytes = m * k + 4 * m * k / 128 + n * k + 4 * (n / 128) * (k / 128) + 2 * m * n
+            qbytes = 2 * m * k + m * k + 4 * m * k / 128
+            ideal = max((qbytes + gbytes) / hbm / 1e6, flops / fp8_burst / 1e9)
+            out[key] = {"path": "fused act-quant + stream-K GEMM (one launch)",
+                        "pair_ms": t, "tflops": flops / t / 1e9,
+                        "gbs": (qbytes + gbytes) / t / 1e6,
+                        "frac_attainable": ideal / t,
+                        "pair_vs_byte_bound": t / ((qbytes + gbytes) / hbm / 1e6),
+                        "bound": "hbm"}
+            continue
         tq = statistics.mean(_ms(ev, key + "_start", key + "_mid"))
         tg = statistics.mean(_ms(ev, key + "_mid", key + "_end"))
         flops = 2.0 * m * n * k
@@ -487,11 +543,14 @@ def _merge_cpu_rows(rows, cpu):
         r = rows.get(key)
         if r is None:
             continue
-        if "cpu_ms" in c:
-            gpu_ms = r.get("ms")
-        else:
-            gpu_ms = (r.get("act_quant_ms", r.get("glue_ms", 0.0)) + r["gemm_ms"])
+        if "cpu_ms" not in c:
             c = dict(c, cpu_ms=c.get("act_quant_cpu_ms", c.get("glue_cpu_ms", 0.0)) + c["gemm_cpu_ms"])
+        if "ms" in r:
+            gpu_ms = r["ms"]
+        elif "pair_ms" in r:
+            gpu_ms = r["pair_ms"]
+        else:
+            gpu_ms = r.get("act_quant_ms", r.get("glue_ms", 0.0)) + r["gemm_ms"]
         r["cpu_baseline"] = dict(c, cores=_cores(), kind="oracle")
         if gpu_ms:
             r["cpu_baseline"]["gpu_speedup"] = c["cpu_ms"] / gpu_ms
@@ -629,6 +688,8 @@ def run_ours(args):
     total_ms, a1_ms = max_over_ranks([total_ms, a1_ms], dev, world)
     rows = _rows(W, ev, args.steps, peaks)
     value = replica_gbs(world, W.req_bytes, args.steps, a1_ms)
+    _decode_paths(W, rows)
+    fp8rl.device_status(local)
 
     # e2e: the same re-quantization through the public API from pinned host
     # buffers (fp8rl_quantize_weights_blockwise_multi_host): host->device copy

@@ -19,6 +19,8 @@ from .binding import (  # noqa: F401
     is_weights_stats,
     is_weights_stats_loss,
     last_error,
+    linear_w8a8_decode,
+    linear_w8a8_decode_workspace_bytes,
     quantize_act_gather,
     quantize_act_groupwise,
     quantize_kv_fp8,

@@ -74,6 +74,9 @@ def load(path: Optional[str] = None):
                                                                        P]),
         "fp8rl_silu_mul_quantize": (ctypes.c_int, [P, i64, i64, i64, P, P, P]),
         "fp8rl_silu_mul_bf16": (ctypes.c_int, [P, i64, i64, i64, P, i64, P]),
+        "fp8rl_linear_w8a8_decode_workspace_bytes": (ctypes.c_size_t, [i64]),
+        "fp8rl_linear_w8a8_decode": (ctypes.c_int, [P, i64, P, P, P, P, i64, i64, i64, P, i64, P,
+                                                    ctypes.c_size_t, P]),
         "fp8rl_decode_attention_fp8kv": (ctypes.c_int, [P, P, P, P, P, P, P, i32, i32, i32, i32,
                                                         i32, i32, i32, f32, P, P]),
         "fp8rl_device_status": (ctypes.c_int, [i32, i32]),
@@ -223,6 +226,50 @@ def gemm_w8a8_blockwise(qa, sa, qw, sw, y: Optional[torch.Tensor] = None, stream
                                             sw.data_ptr(), m, n, k, y.data_ptr(), y.stride(0),
                                             _stream(stream)))
     return y
+
+
+def linear_w8a8_decode_workspace_bytes(n: int) -> int:
+    """Workspace bytes linear_w8a8_decode needs for n output columns on the
+    current device."""
+    return int(load().fp8rl_linear_w8a8_decode_workspace_bytes(int(n)))
+
+
+def linear_w8a8_decode(a, qw, sw, y: Optional[torch.Tensor] = None,
+                       qa: Optional[torch.Tensor] = None, sa: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None):
+    """Decode-sized linear layer (m <= 256): quantize bf16 a [m, k] in 1x128
+    groups and multiply by the E4M3 weights in one launch.  Returns (y, qa, sa).
+    With a=None, qa/sa are the (already quantized) inputs.  workspace: a
+    zero-filled uint8 device tensor of linear_w8a8_decode_workspace_bytes(n)
+    bytes, reusable across calls (allocated here when None)."""
+    _dev(qw, torch.uint8, "qw"); _dev(sw, torch.float32, "sw")
+    n, k = qw.shape
+    dev = qw.device
+    if a is not None:
+        _rowmajor(_dev(a, torch.bfloat16, "a"), "a")
+        m = a.shape[0]
+        if qa is None:
+            qa = torch.empty(m, k, dtype=torch.uint8, device=dev)
+        if sa is None:
+            sa = torch.empty(k // 128, m, dtype=torch.float32, device=dev)
+    else:
+        if qa is None or sa is None:
+            raise ValueError("without a, qa and sa are required")
+        m = qa.shape[0]
+    _dev(qa, torch.uint8, "qa"); _dev(sa, torch.float32, "sa")
+    if y is None:
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+    _rowmajor(_dev(y, torch.bfloat16, "y"), "y")
+    if workspace is None:
+        workspace = torch.zeros(linear_w8a8_decode_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    _dev(workspace, torch.uint8, "workspace")
+    _check(load().fp8rl_linear_w8a8_decode(a.data_ptr() if a is not None else None,
+                                           a.stride(0) if a is not None else k,
+                                           qa.data_ptr(), sa.data_ptr(), qw.data_ptr(),
+                                           sw.data_ptr(), m, n, k, y.data_ptr(), y.stride(0),
+                                           workspace.data_ptr(), workspace.numel(),
+                                           _stream(stream)))
+    return y, qa, sa
 
 
 def grouped_gemm_w8a8_blockwise(qa, sa, qw, sw, offsets, y: Optional[torch.Tensor] = None,

@@ -131,6 +131,40 @@ fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float* sa, const
                                        const float* sw, int64_t m, int64_t n, int64_t k,
                                        void* y, int64_t ldy, cudaStream_t stream);
 
+/* Decode-sized linear layer: the 1x128 activation quantization fused with
+ * the blockwise W8A8 GEMM, for m <= 256 rows (a decode batch).  Section 3.4.2
+ * Phase 3: each decode step quantizes its activations dynamically and
+ * multiplies them by the per-step FP8 weights on FP8 tensor cores, FP32
+ * accumulation, BF16 output.  Results:
+ *   qa, sa   exactly fp8rl_quantize_act_groupwise(a) (bit for bit)
+ *   y        Y = A W^T as fp8rl_gemm_w8a8_blockwise defines it, to the same
+ *            accuracy (the FP32 partial sums of a tile may be added in another
+ *            order; the order is fixed, so results repeat bit for bit).
+ * One cooperative launch over every SM: the CTAs quantize A together, meet at
+ * a grid barrier, then split the (128-column tile, 128-deep k-block) units of
+ * the GEMM evenly ("stream-K"); a tile shared by several CTAs is reduced by
+ * the last one to finish it, in k order, through `workspace`.
+ *   a        BF16 [m, k], row stride lda (>= k, multiple of 8), 16-byte
+ *            aligned; NULL: qa and sa are inputs (already quantized A) and
+ *            the call is the stream-K GEMM alone
+ *   qa       E4M3 [m, k] dense, 16-byte aligned (written when a != NULL)
+ *   sa       FP32 [k/128, m] group-major (written when a != NULL)
+ *   qw, sw   E4M3 [n, k] and FP32 [n/128, k/128], as in the dense GEMM
+ *   y        BF16 [m, n], row stride ldy (>= n, multiple of 8), 16-byte aligned
+ *   workspace  DEVICE memory owned by the caller, 256-byte aligned, at least
+ *            fp8rl_linear_w8a8_decode_workspace_bytes(n) bytes, ZERO-FILLED
+ *            before its first use.  The call leaves its counters at zero
+ *            again, so a workspace can be reused by later calls; calls that
+ *            overlap on the GPU need separate workspaces.  After a call that
+ *            reported FP8RL_ERR_TIMEOUT, zero it again.
+ * Requires 0 <= m <= 256, n a positive multiple of 128, k a positive
+ * multiple of 128; m = 0 is a no-op. */
+size_t fp8rl_linear_w8a8_decode_workspace_bytes(int64_t n);
+fp8rl_status fp8rl_linear_w8a8_decode(const void* a, int64_t lda, uint8_t* qa, float* sa,
+                                      const uint8_t* qw, const float* sw, int64_t m, int64_t n,
+                                      int64_t k, void* y, int64_t ldy, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream);
+
 /* Grouped (MoE expert) variant: rows [offsets[e], offsets[e+1]) of A are the
  * tokens routed to expert e (section 3.4.1 "MoE expert layers: fc1, fc2") and
  * are multiplied by expert e's weights.

@@ -111,3 +111,17 @@ def test_error_path_entries_check_their_arguments_on_the_host(lib):
     assert "unknown status flags" in binding.last_error()
     assert lib.fp8rl_selftest_bounded_wait(0, None) == 1            # limit out of range
     assert lib.fp8rl_selftest_bounded_wait(1000001, None) == 1
+
+
+def test_decode_linear_checks_shapes_on_the_host(lib):
+    fake = 1 << 20          # never dereferenced: the call fails its checks first
+    f = lib.fp8rl_linear_w8a8_decode
+    # m > 256
+    assert f(fake, 128, fake, fake, fake, fake, 257, 128, 128, fake, 128, 1 << 12, 1 << 30, None) == 3
+    # n not a multiple of 128
+    assert f(fake, 128, fake, fake, fake, fake, 16, 200, 128, fake, 200, 1 << 12, 1 << 30, None) == 3
+    # null workspace
+    assert f(fake, 128, fake, fake, fake, fake, 16, 128, 128, fake, 128, None, 1 << 30, None) == 1
+    # misaligned workspace
+    assert f(fake, 128, fake, fake, fake, fake, 16, 128, 128, fake, 128, (1 << 12) + 16, 1 << 30,
+             None) == 2
