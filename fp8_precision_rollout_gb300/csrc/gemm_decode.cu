@@ -22,10 +22,11 @@
 //     sa * sw into FP32 registers as in the dense kernel;
 //   * a CTA that owns a whole tile stores it as BF16; otherwise it writes its
 //     FP32 partial to its slot of the caller's workspace and counts itself in
-//     the tile's arrival counter.  The CTA whose arrival completes the count
-//     adds the tile's partials in k order (segment 0 first, its own in its
-//     place), so the result does not depend on arrival order, stores BF16 and
-//     returns the counter to zero.  No CTA waits for another here.
+//     the tile's arrival counter.  After its main loop each CTA of a split
+//     tile waits for the tile's partials, then adds them in k order (segment 0
+//     first) for its share of the tile's rows and stores BF16, so the result
+//     does not depend on arrival order and the reduction is spread over the
+//     tile's CTAs.  The last CTA out returns the counters to zero.
 //
 // Shape: 11 warps.  Warp 0 lane 0: TMA producer (4 stages of 48 KB: A 256 x 128
 // + W 128 x 128 bytes, 128-byte swizzle).  Warps 1-2 lane 0: MMA issuers,
@@ -66,7 +67,6 @@ struct DecodeTail {
   uint32_t tmem_base;
   uint32_t abort_flag;
   uint32_t a_ready;
-  uint32_t last;
   uint32_t stop;
 };
 constexpr size_t kDTailPad = (sizeof(DecodeTail) + 1023) / 1024 * 1024;
@@ -83,7 +83,8 @@ struct DecodeArgs {
   int64_t ldy;
   int M, N, KB, n_tiles;
   float* partials;       // [2 G] slots of [32 chunks][256 rows][4 floats]
-  uint32_t* tile_ctr;    // [n_tiles] arrivals per tile (zero between calls)
+  uint32_t* arrive;      // [n_tiles] partials published per split tile (zero between calls)
+  uint32_t* done;        // [n_tiles] CTAs done reducing per split tile (zero between calls)
   uint32_t* grid_bar;    // [0] arrivals, [1] generation
   uint32_t* status;
 };
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       mbar_init(smem_u32(&st->tempty[b]), 8);
     }
     st->abort_flag = 0;
+    st->stop = 0;
     st->a_ready = g.a ? 0u : 1u;
     mbar_fence_init();
     tma_prefetch_map(&tmA);
@@ -360,6 +362,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
       bool alive = true;
       int i = 0;   // unit index within this CTA
       int64_t u = u0;
+      int split[2];      // this CTA's split tiles (only the ends of its range can be)
+      int n_split = 0;
       while (u < u1) {
         const int t = (int)(u / KB);
         const int ka = (int)(u - (int64_t)t * KB);
@@ -429,61 +433,108 @@ __global__ void __launch_bounds__(kDThreads, 1)
             }
           }
         } else {
-          // partial tile: publish it, count this CTA in, and let the CTA that
-          // completes the count reduce in segment (k) order
+          // partial tile: publish it and count this CTA in; the tile is
+          // reduced after the main loop (below)
           float* mine = g.partials + (size_t)slot_of(c, t, U, G, KB) * kPartialFloats;
 #pragma unroll
           for (int cc = 0; cc < DN / 4; ++cc)
             __stcg(reinterpret_cast<float4*>(mine + ((size_t)cc * DM + row) * 4),
                    make_float4(acc[cc * 4], acc[cc * 4 + 1], acc[cc * 4 + 2], acc[cc * 4 + 3]));
-          __threadfence();
+          // the barrier orders every thread's stores before thread 96's fence
+          // and release (fences are cumulative), so one fence suffices
           named_bar(1, 256);
-          const int cf = owner_of((int64_t)t * KB, U, G);
-          const int cl = owner_of((int64_t)t * KB + KB - 1, U, G);
-          const int nseg = cl - cf + 1;
           if (tid == 96) {
-            const uint32_t old = atomicAdd(g.tile_ctr + t, 1u);
-            const bool last = old == (uint32_t)nseg - 1u;
-            if (last) g.tile_ctr[t] = 0u;   // no other CTA touches it again in this launch
-            st->last = last ? 1u : 0u;
-          }
-          named_bar(1, 256);
-          if (st->last) {
             __threadfence();
-            const int myseg = c - cf;
-            if (row_ok) {
-#pragma unroll
-              for (int cc = 0; cc < DN / 4; ++cc) {
-                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int j = 0; j < nseg; ++j) {
-                  float4 v;
-                  if (j == myseg) {
-                    v = make_float4(acc[cc * 4], acc[cc * 4 + 1], acc[cc * 4 + 2], acc[cc * 4 + 3]);
-                  } else {
-                    const float* other = g.partials + (size_t)slot_of(cf + j, t, U, G, KB) * kPartialFloats;
-                    v = __ldcg(reinterpret_cast<const float4*>(other + ((size_t)cc * DM + row) * 4));
-                  }
-                  if (j == 0) {
-                    sum = v;
-                  } else {
-                    sum.x = __fadd_rn(sum.x, v.x);
-                    sum.y = __fadd_rn(sum.y, v.y);
-                    sum.z = __fadd_rn(sum.z, v.z);
-                    sum.w = __fadd_rn(sum.w, v.w);
-                  }
-                }
-                __nv_bfloat162 b0 = __floats2bfloat162_rn(sum.x, sum.y);
-                __nv_bfloat162 b1 = __floats2bfloat162_rn(sum.z, sum.w);
-                uint2 o;
-                o.x = *reinterpret_cast<uint32_t*>(&b0);
-                o.y = *reinterpret_cast<uint32_t*>(&b1);
-                *reinterpret_cast<uint2*>(yrow + cc * 4) = o;
-              }
-            }
+            atomicAdd(g.arrive + t, 1u);
           }
-          named_bar(1, 256);   // st->last is reused by the next segment
+          split[n_split++] = t;
         }
         u += kz - ka;
+      }
+      // ------------------------------------------------- split tiles ------
+      // Every CTA publishes its partials during its main loop and waits for
+      // nothing there, so each split tile's partials all arrive.  Here each
+      // CTA of a split tile waits (bounded) for them, then sums its share of
+      // the tile's rows over the tile's CTAs in k order (the result does not
+      // depend on arrival order) and stores BF16.  All CTAs are resident
+      // (cooperative launch), so the waits end.
+      for (int p = 0; p < n_split && !st->stop; ++p) {
+        const int t = split[p];
+        const int cf = owner_of((int64_t)t * KB, U, G);
+        const int nseg = owner_of((int64_t)t * KB + KB - 1, U, G) - cf + 1;
+        const int myseg = c - cf;
+        if (tid == 96) {
+          volatile uint32_t* arr = g.arrive + t;
+          const uint64_t t0 = gtimer();
+          bool ok = true;
+          for (uint32_t it = 1; *arr < (uint32_t)nseg; ++it) {
+            if ((it & 63u) == 0 && (*abort_flag || gtimer() - t0 > kWaitLimitNs)) {
+              if (!*abort_flag) {
+                atomicOr(g.status, kStatusTimeout);
+                atomicExch(g.status + 1, 48u);
+                *abort_flag = 1u;
+              }
+              ok = false;
+              break;
+            }
+          }
+          __threadfence();
+          st->stop = ok ? 0u : 1u;
+        }
+        named_bar(1, 256);
+        if (st->stop) break;
+        const int r0 = (DM * myseg) / nseg;
+        const int r1 = min((DM * (myseg + 1)) / nseg, g.M);
+        const int nrows = max(r1 - r0, 0);
+        const int nel = nrows * (DN / 4);            // float4 elements of the share (<= 4096)
+        const int et = tid - 96;
+        constexpr int kEl = 16;                        // per thread; a partial's loads go out together
+        float4 sum[kEl];
+        for (int j = 0; j < nseg; ++j) {
+          const float* pj = g.partials + (size_t)slot_of(cf + j, t, U, G, KB) * kPartialFloats;
+          float4 v[kEl];
+#pragma unroll
+          for (int e = 0; e < kEl; ++e) {
+            const int idx = et + e * 256;
+            v[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (idx < nel) {
+              const int cc = idx / nrows, r = r0 + idx % nrows;
+              v[e] = __ldcg(reinterpret_cast<const float4*>(pj + ((size_t)cc * DM + r) * 4));
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < kEl; ++e) {
+            if (j == 0) {
+              sum[e] = v[e];
+            } else {
+              sum[e].x = __fadd_rn(sum[e].x, v[e].x);
+              sum[e].y = __fadd_rn(sum[e].y, v[e].y);
+              sum[e].z = __fadd_rn(sum[e].z, v[e].z);
+              sum[e].w = __fadd_rn(sum[e].w, v[e].w);
+            }
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < kEl; ++e) {
+          const int idx = et + e * 256;
+          if (idx < nel) {
+            const int cc = idx / nrows, r = r0 + idx % nrows;
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(sum[e].x, sum[e].y);
+            __nv_bfloat162 b1 = __floats2bfloat162_rn(sum[e].z, sum[e].w);
+            uint2 o;
+            o.x = *reinterpret_cast<uint32_t*>(&b0);
+            o.y = *reinterpret_cast<uint32_t*>(&b1);
+            *reinterpret_cast<uint2*>(g.y + (int64_t)r * g.ldy + (int64_t)t * DN + cc * 4) = o;
+          }
+        }
+        named_bar(1, 256);
+        if (tid == 96) {
+          // the tile's last CTA out returns both counters to zero
+          if (atomicAdd(g.done + t, 1u) == (uint32_t)nseg - 1u) {
+            g.arrive[t] = 0u;
+            g.done[t] = 0u;
+          }
+        }
       }
     }
   }
@@ -529,8 +580,10 @@ fp8rl_status decode_device(const DeviceState* ds, DecodeDevice* out) {
   return FP8RL_OK;
 }
 
+size_t counters_bytes(int64_t n_tiles) { return (size_t)((4 * n_tiles + 255) / 256) * 256; }
+
 size_t workspace_bytes_for(int grid, int64_t n_tiles) {
-  const size_t ctl = 256 + (size_t)((4 * n_tiles + 255) / 256) * 256;
+  const size_t ctl = 256 + 2 * counters_bytes(n_tiles);
   return ctl + (size_t)2 * grid * kPartialFloats * sizeof(float);
 }
 
@@ -593,8 +646,9 @@ extern "C" fp8rl_status fp8rl_linear_w8a8_decode(const void* a, int64_t lda, uin
   g.n_tiles = (int)n_tiles;
   char* ws = static_cast<char*>(workspace);
   g.grid_bar = reinterpret_cast<uint32_t*>(ws);
-  g.tile_ctr = reinterpret_cast<uint32_t*>(ws + 256);
-  g.partials = reinterpret_cast<float*>(ws + 256 + ((4 * n_tiles + 255) / 256) * 256);
+  g.arrive = reinterpret_cast<uint32_t*>(ws + 256);
+  g.done = reinterpret_cast<uint32_t*>(ws + 256 + counters_bytes(n_tiles));
+  g.partials = reinterpret_cast<float*>(ws + 256 + 2 * counters_bytes(n_tiles));
   g.status = ds->status;
   // At most one CTA per unit, so that every CTA owns at least one: then the
   // CTAs from a tile's first owner to its last all hold part of it, and the

@@ -10,6 +10,8 @@ Cases (device footprint in parentheses):
   gemm_prefill    act-quant'ed W8A8 GEMM, gate_up shape M=8192 N=24576 K=4096 (0.6 GB)
   gemm_decode     W8A8 GEMM, qkv shape M=256 N=6144 K=4096 (0.03 GB)
   gemm_decode_o   W8A8 GEMM, o shape M=256 N=4096 K=4096 (0.02 GB; split-K clusters of 2)
+  linear_decode   fused act-quant + stream-K W8A8 GEMM, qkv shape M=256 N=6144 K=4096 (0.03 GB)
+  linear_decode_o the same, o shape M=256 N=4096 K=4096 (0.02 GB)
   grouped         grouped W8A8 GEMM, Qwen3-30B-A3B gate_up, 128 experts (0.5 GB)
   kv              KV calibrate + quantize, 8 x 20480 tokens x 8 x 128 (0.5 GB)
   tis             TIS weights over 64 x 20480 tokens (0.02 GB)
@@ -59,6 +61,15 @@ def main(argv=None):
         qw, sw = fp8rl.quantize_weights_blockwise(wl.make_weight(n, k, seed=3, device=dev))
         y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
         run = lambda: fp8rl.gemm_w8a8_blockwise(qa, sa, qw, sw, y)  # noqa: E731
+    elif c in ("linear_decode", "linear_decode_o"):
+        m, n, k = (256, 6144, 4096) if c == "linear_decode" else (256, 4096, 4096)
+        a = wl.dense_acts(m, k, seed=2, device=dev)
+        qw, sw = fp8rl.quantize_weights_blockwise(wl.make_weight(n, k, seed=3, device=dev))
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        qa = torch.empty(m, k, dtype=torch.uint8, device=dev)
+        sa = torch.empty(k // 128, m, dtype=torch.float32, device=dev)
+        ws = torch.zeros(fp8rl.linear_w8a8_decode_workspace_bytes(n), dtype=torch.uint8, device=dev)
+        run = lambda: fp8rl.linear_w8a8_decode(a, qw, sw, y, qa, sa, ws)  # noqa: E731
     elif c == "grouped":
         off, _, _ = wl.moe_routing(seed=0)
         rows = int(off[-1])
