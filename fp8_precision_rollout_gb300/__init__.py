@@ -32,4 +32,6 @@ from .binding import (  # noqa: F401
     silu_mul_quantize,
     tis_weights,
     version,
+    weight_shard_rows,
 )
+from . import weight_sync  # noqa: F401

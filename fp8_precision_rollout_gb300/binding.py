@@ -80,6 +80,7 @@ def load(path: Optional[str] = None):
         "fp8rl_decode_attention_fp8kv": (ctypes.c_int, [P, P, P, P, P, P, P, i32, i32, i32, i32,
                                                         i32, i32, i32, f32, P, P]),
         "fp8rl_device_status": (ctypes.c_int, [i32, i32]),
+        "fp8rl_weight_shard_rows": (ctypes.c_int, [i64, i32, i32, P, P]),
         "fp8rl_inject_device_status": (ctypes.c_int, [i32, ctypes.c_uint32, ctypes.c_uint32]),
         "fp8rl_selftest_bounded_wait": (ctypes.c_int, [i32, P]),
     }
@@ -526,3 +527,12 @@ def inject_device_status(device: int, flags: int, site: int = 0):
 def selftest_bounded_wait(limit_us: int, stream=None):
     """Launch the bounded-wait self-test kernel (its wait times out; see fp8rl.h)."""
     _check(load().fp8rl_selftest_bounded_wait(int(limit_us), _stream(stream)))
+
+
+def weight_shard_rows(n: int, world: int, rank: int):
+    """Rows [begin, end) of an n-row weight owned by `rank` in the sharded
+    weight sync (whole 128-row block bands; see fp8rl.h)."""
+    b, e = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().fp8rl_weight_shard_rows(int(n), int(world), int(rank), ctypes.byref(b),
+                                          ctypes.byref(e)))
+    return b.value, e.value

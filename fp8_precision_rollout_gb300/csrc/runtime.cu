@@ -2,6 +2,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdarg>
+#include <algorithm>
 #include <cstdio>
 #include <mutex>
 #include <string>
@@ -202,4 +203,18 @@ extern "C" fp8rl_status fp8rl_selftest_bounded_wait(int32_t limit_us, cudaStream
   bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(ds->status, (uint64_t)limit_us * 1000ull);
   st = cuda_check(cudaGetLastError(), "bounded_wait_selftest_kernel launch");
   return st == FP8RL_OK ? ok() : st;
+}
+
+// ------------------------------------------------ sharded weight sync plan --
+
+extern "C" fp8rl_status fp8rl_weight_shard_rows(int64_t n, int32_t world, int32_t rank,
+                                                int64_t* row_begin, int64_t* row_end) {
+  if (!row_begin || !row_end) return fail(FP8RL_ERR_INVALID_ARG, "null pointer");
+  if (n < 0 || world < 1 || rank < 0 || rank >= world)
+    return fail(FP8RL_ERR_INVALID_ARG, "need n >= 0, world >= 1 and 0 <= rank < world");
+  const int64_t blocks = (n + 127) / 128;
+  const int64_t b0 = blocks * rank / world, b1 = blocks * (rank + 1) / world;
+  *row_begin = std::min<int64_t>(b0 * 128, n);
+  *row_end = std::min<int64_t>(b1 * 128, n);
+  return ok();
 }

@@ -386,6 +386,19 @@ fp8rl_status fp8rl_is_weights_stats_loss(const float* logp_train, const float* l
  * ordinal. */
 fp8rl_status fp8rl_device_status(int32_t device, int32_t clear);
 
+/* Shard plan of the sharded weight synchronization (section 3.4.2 Phase 2:
+ * the trainer's FSDP shards are gathered and quantized before they reach the
+ * engine).  Here each rank quantizes its own rows first and the ranks then
+ * all-gather the E4M3 codes and FP32 scales, about half the bytes of a BF16
+ * gather.  Rank `rank` of `world` owns rows [*row_begin, *row_end) of an
+ * n-row weight: a contiguous run of whole 128-row block bands (the bands are
+ * dealt as evenly as possible, in rank order), so no 128 x 128 block crosses
+ * two ranks and the gathered codes and scales equal those of the whole
+ * tensor bit for bit.  A rank may own no rows (begin == end).  Host-only: no
+ * device is touched. */
+fp8rl_status fp8rl_weight_shard_rows(int64_t n, int32_t world, int32_t rank, int64_t* row_begin,
+                                     int64_t* row_end);
+
 /* Error-path support (no counterpart in the pages): lets a caller's tests
  * exercise its handling of fp8rl_device_status without faulting a GPU.
  * fp8rl_inject_device_status synchronizes `device` and overwrites its status
