@@ -206,10 +206,10 @@ __device__ __noinline__ uint32_t silu_mul_bf16_general(uint32_t gb, uint32_t ub)
   return sx | bits;
 }
 
-// y = BF16_RNE(silu(g) * u) for BF16 bit patterns gb, ub (low 16 bits).
-// Fast path: a natural entry with |hi * u| >= 2^-100 (then hi*u - p is exact).
-__device__ __forceinline__ uint32_t silu_mul_bf16(uint32_t gb, uint32_t ub) {
-  const float hi = __ldg(&g_silu_hi[gb]);
+// y = BF16_RNE(silu(g) * u) for BF16 bit patterns gb, ub (low 16 bits), with
+// hi = g_silu_hi[gb] already loaded.  Fast path: a natural entry with
+// |hi * u| >= 2^-100 (then hi*u - p is exact).
+__device__ __forceinline__ uint32_t silu_mul_bf16_hi(uint32_t gb, uint32_t ub, float hi) {
   const float u = __uint_as_float(ub << 16);
   const float p = fx::fmul(hi, u);
   if (fabsf(p) >= 0x1p-100f) {
@@ -231,10 +231,24 @@ __device__ __forceinline__ uint32_t silu_mul_bf16(uint32_t gb, uint32_t ub) {
   return silu_mul_bf16_general(gb, ub);
 }
 
-// Two BF16 lanes (packed in a 32-bit word) of gate and up -> the packed BF16
-// pair silu(g) * u.
-__device__ __forceinline__ uint32_t silu_mul2(uint32_t g2, uint32_t u2) {
-  return silu_mul_bf16(g2 & 0xFFFFu, u2 & 0xFFFFu) | (silu_mul_bf16(g2 >> 16, u2 >> 16) << 16);
+// 8 outputs from a 16-byte vector of gates and one of ups.  The 8 table
+// lookups are issued before any of them is used (their latency, not the
+// arithmetic, sets the kernels' pace).
+__device__ __forceinline__ uint4 silu_mul8(const uint4& gv, const uint4& uv) {
+  const uint32_t g[4] = {gv.x, gv.y, gv.z, gv.w};
+  const uint32_t u[4] = {uv.x, uv.y, uv.z, uv.w};
+  float hi[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    hi[2 * j] = __ldg(&g_silu_hi[g[j] & 0xFFFFu]);
+    hi[2 * j + 1] = __ldg(&g_silu_hi[g[j] >> 16]);
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    o[j] = silu_mul_bf16_hi(g[j] & 0xFFFFu, u[j] & 0xFFFFu, hi[2 * j]) |
+           (silu_mul_bf16_hi(g[j] >> 16, u[j] >> 16, hi[2 * j + 1]) << 16);
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // y[r, c] = BF16_RNE(silu(h[r, c]) * h[r, inter + c]); 8 outputs per thread
@@ -248,16 +262,14 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t* __restric
     const int64_t r = v / vpr, c = (v - r * vpr) * 8;
     const uint4 gv = ld_stream(h + r * ldh + c);
     const uint4 uv = ld_stream(h + r * ldh + inter + c);
-    *reinterpret_cast<uint4*>(y + r * ldy + c) =
-        make_uint4(silu_mul2(gv.x, uv.x), silu_mul2(gv.y, uv.y), silu_mul2(gv.z, uv.z),
-                   silu_mul2(gv.w, uv.w));
+    *reinterpret_cast<uint4*>(y + r * ldy + c) = silu_mul8(gv, uv);
   }
 }
 
 // Gated activation + 1x128 quantization: the task layout of aquant_kernel
 // over the [m, inter] output; each lane forms its 4 x 8 outputs from the
 // gate and up halves of its row, then quantizes them like aquant_kernel.
-__global__ void __launch_bounds__(256) silu_quant_kernel(const uint16_t* __restrict__ h, int64_t m,
+__global__ void __launch_bounds__(256, 3) silu_quant_kernel(const uint16_t* __restrict__ h, int64_t m,
                                                          int64_t inter, int64_t ldh,
                                                          uint8_t* __restrict__ q,
                                                          float* __restrict__ scales,
@@ -274,19 +286,21 @@ __global__ void __launch_bounds__(256) silu_quant_kernel(const uint16_t* __restr
     const int g = (int)(f - r * kb);
     const int64_t gcol = (int64_t)g * 128;
     const uint16_t* hrow = h + r * ldh;
+    uint4 gv[4], uv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t col = gcol + (slot + 4 * i) * 8;
+      if (valid && col < inter) {
+        gv[i] = ld_stream(hrow + col);
+        uv[i] = ld_stream(hrow + inter + col);
+      }
+    }
     uint4 v[4];
     uint32_t m2 = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t col = gcol + (slot + 4 * i) * 8;
-      if (valid && col < inter) {
-        const uint4 gv = ld_stream(hrow + col);
-        const uint4 uv = ld_stream(hrow + inter + col);
-        v[i] = make_uint4(silu_mul2(gv.x, uv.x), silu_mul2(gv.y, uv.y), silu_mul2(gv.z, uv.z),
-                          silu_mul2(gv.w, uv.w));
-      } else {
-        v[i] = make_uint4(0, 0, 0, 0);
-      }
+      v[i] = (valid && col < inter) ? silu_mul8(gv[i], uv[i]) : make_uint4(0, 0, 0, 0);
       m2 = absmax8(m2, v[i]);
     }
     const float amax = warp_max(bf16x2_maxf(m2), 4);
