@@ -23,6 +23,14 @@
 namespace fp8rl {
 namespace {
 
+// Programmatic dependent launch: lets the next kernel in the stream, if it was
+// launched with programmatic serialization allowed (the GEMMs are), start its
+// launch and prologue now.  It still waits (griddepcontrol.wait) for this
+// grid to complete before it reads memory, so this changes timing only.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------ 1x128 activation groups --
 
 // Groups are numbered row-major over the whole matrix, f = r * kb + g (kb =
@@ -40,6 +48,7 @@ __global__ void __launch_bounds__(256) aquant_kernel(const uint16_t* __restrict_
                                                      int64_t n_tasks, int kb,
                                                      const int32_t* __restrict__ rows,
                                                      int64_t m_src, uint32_t* status) {
+  allow_dependent_launch();   // the GEMM that reads these codes may launch now
   const int lane = threadIdx.x & 31;
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -274,6 +283,7 @@ __global__ void __launch_bounds__(256, 3) silu_quant_kernel(const uint16_t* __re
                                                          uint8_t* __restrict__ q,
                                                          float* __restrict__ scales,
                                                          int64_t n_tasks, int kb) {
+  allow_dependent_launch();   // the grouped GEMM that reads these codes may launch now
   const int lane = threadIdx.x & 31;
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
