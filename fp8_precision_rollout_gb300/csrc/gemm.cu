@@ -62,32 +62,47 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMGroup = 16;                      // m-tiles per raster band (L2 reuse)
 constexpr int kMaxStages = 6;
 
-// The two tile flavours.  Wide (dense and grouped): 128 x 256 tiles, 3 stages
-// of 48 KB, and the freed 48 KB spent on output staging so the epilogue never
-// waits for its previous tile's stores.  Split-K (decode shapes): 128 x 128
-// tiles and 6 stages of 32 KB, the same 192 KB, to keep more DRAM reads in
-// flight.
-template <bool kSplit>
+// The tile flavours.
+//   Wide (kWide; grouped GEMMs): 128 x 256 tiles, 3 stages of 48 KB, two TMEM
+//     partial buffers, and 64 KB of output staging so the epilogue never waits
+//     for its previous tile's stores.
+//   Split-K (kSplitK; decode shapes): 128 x 128 tiles and 6 stages of 32 KB,
+//     to keep more DRAM reads in flight; partials reduced across a cluster.
+//   Narrow (kNarrow; dense GEMMs with many tiles): 128 x 128 tiles, 5 stages
+//     of 32 KB, FOUR TMEM partial buffers and 32 KB of output staging.  With
+//     two buffers, a buffer's promotion, the warps' skew and its release
+//     take longer than the other buffer's MMAs, so the tensor pipe waits
+//     every k-block; four buffers let the MMAs run three k-blocks ahead.
+//     (Stages >= buffers: a stage's previous use is always a k-block whose
+//     buffer the epilogue has released before its next wait can start.)
+constexpr int kWide = 0, kSplitK = 1, kNarrow = 2;
+template <int kF>
 struct Flavour {
-  static constexpr int kBN = kSplit ? 128 : 256;
-  static constexpr int kStages = kSplit ? 6 : 3;
+  static constexpr int kBN = kF == kWide ? 256 : 128;
+  static constexpr int kStages = kF == kWide ? 3 : (kF == kSplitK ? 6 : 5);
+  static constexpr int kBufs = kF == kNarrow ? 4 : 2;   // TMEM partial buffers
+  static constexpr bool kStaged = kF != kSplitK;          // TMA output staging
   static constexpr int kBStage = kBN * BK;
   static constexpr int kStageBytes = kAStage + kBStage;
   static constexpr int kHalf = kBN / 2;             // columns per epilogue warp
-  static constexpr uint32_t kTmemCols = 2 * kBN;    // two partial buffers
+  static constexpr int kBoxes = kHalf / 64;         // 32 x 64 output boxes per warp
+  static constexpr uint32_t kTmemCols = kBufs * kBN;
   // tcgen05 instruction descriptor, kind::f8f6f4: D = F32 (bits 4-5 = 1),
   // A = B = E4M3 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0),
   // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
   static constexpr uint32_t kIdesc =
       (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 };
-static_assert(Flavour<false>::kStages <= kMaxStages && Flavour<true>::kStages <= kMaxStages, "");
+static_assert(Flavour<kWide>::kStages <= kMaxStages && Flavour<kSplitK>::kStages <= kMaxStages &&
+                  Flavour<kNarrow>::kStages <= kMaxStages && Flavour<kNarrow>::kStages >= Flavour<kNarrow>::kBufs,
+              "");
+static_assert(Flavour<kNarrow>::kTmemCols <= 512 && Flavour<kWide>::kTmemCols <= 512, "TMEM columns");
 
 struct SharedTail {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull[4];
+  uint64_t tempty[4];
   uint32_t tmem_base;
   uint32_t abort_flag;
   int32_t total_tiles;
@@ -102,24 +117,26 @@ struct SharedTail {
 // Y tensor map describes; after the tail, 1 KB aligned.
 constexpr int kYBox = 32, kYBoxCols = 64;
 constexpr int kYBoxBytes = kYBox * kYBoxCols * 2;
-constexpr int kYWarpBytes = 2 * kYBoxBytes;
 constexpr size_t kTailPad = (sizeof(SharedTail) + 1023) / 1024 * 1024;
-constexpr size_t smem_bytes(bool split) {
-  return split ? 1024 + (size_t)Flavour<true>::kStages * Flavour<true>::kStageBytes + kTailPad
-               : 1024 + (size_t)Flavour<false>::kStages * Flavour<false>::kStageBytes + kTailPad +
-                     8 * (size_t)kYWarpBytes;
+template <int kF>
+constexpr size_t smem_bytes() {
+  using F = Flavour<kF>;
+  return 1024 + (size_t)F::kStages * F::kStageBytes + kTailPad +
+         (F::kStaged ? 8 * (size_t)F::kBoxes * kYBoxBytes : 0);
 }
-static_assert(smem_bytes(false) <= 232448 && smem_bytes(true) <= 232448, "shared memory budget");
+static_assert(smem_bytes<kWide>() <= 232448 && smem_bytes<kSplitK>() <= 232448 &&
+                  smem_bytes<kNarrow>() <= 232448,
+              "shared memory budget");
 
 // Split-K flavour: a cluster owns exactly one tile, so once its last MMA has
 // completed the stage buffers are idle and hold the FP32 partial tile,
 // [128 rows][kRedLd] (row pitch 528 B: 16-byte stores by consecutive rows
 // and 16-byte loads along a row are both bank-conflict free).
-constexpr int kRedLd = Flavour<true>::kBN + 4;
+constexpr int kRedLd = Flavour<kSplitK>::kBN + 4;
 constexpr int kMaxSplit = 4;
 constexpr int kRedBatch = 4;             // row chunks whose loads are in flight together
 static_assert((size_t)BM * kRedLd * sizeof(float) <=
-                  (size_t)Flavour<true>::kStages * Flavour<true>::kStageBytes,
+                  (size_t)Flavour<kSplitK>::kStages * Flavour<kSplitK>::kStageBytes,
               "the partial tile must fit in the stage buffers");
 
 struct GemmArgs {
@@ -257,7 +274,7 @@ __device__ __forceinline__ void reduce_rows(uint32_t red, int crank, int nsplit,
                                             int row_end, int n0, const GemmArgs& g, int et) {
   const int lo = (BM * crank) / nsplit;
   const int hi = min((BM * (crank + 1)) / nsplit, row_end - m0);
-  constexpr int kV = Flavour<true>::kBN / 4;   // 16-byte vectors per row
+  constexpr int kV = Flavour<kSplitK>::kBN / 4;   // 16-byte vectors per row
   const int tasks = (hi - lo) * kV;
   uint32_t base[kMaxSplit];
 #pragma unroll
@@ -308,12 +325,14 @@ __device__ __forceinline__ void reduce_rows(uint32_t red, int crank, int nsplit,
 // are too few tiles to fill the GPU (decode-sized M); two cluster barrier
 // phases order it: (A) every partial is staged, (B) no CTA reads a peer's
 // shared memory any more (waited for only just before leaving).
-template <bool kGrouped, bool kSplit>
+template <bool kGrouped, int kF>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmY, const GemmArgs g) {
-  using F = Flavour<kSplit>;
+  using F = Flavour<kF>;
+  constexpr bool kSplit = kF == kSplitK;
   constexpr int STAGES = F::kStages;
+  constexpr int BUFS = F::kBufs;
   constexpr int kBN = F::kBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -322,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + STAGES * kAStage;
   SharedTail* st = reinterpret_cast<SharedTail*>(smem + STAGES * F::kStageBytes);
   float* red = reinterpret_cast<float*>(smem);   // split-K: aliases the idle stage buffers
-  uint8_t* ystage = smem + STAGES * F::kStageBytes + kTailPad;   // unused by split-K
+  uint8_t* ystage = smem + STAGES * F::kStageBytes + kTailPad;   // staged flavours only
   volatile uint32_t* abort_flag = &st->abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -339,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&st->full[s]), 1);
       mbar_init(smem_u32(&st->empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < BUFS; ++b) {
       mbar_init(smem_u32(&st->tfull[b]), 1);
       mbar_init(smem_u32(&st->tempty[b]), 8);
     }
@@ -348,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
-    if (!kSplit) tma_prefetch_map(&tmY);
+    if (F::kStaged) tma_prefetch_map(&tmY);
   }
   // The launch allows programmatic serialization: the launch itself and the
   // set-up above (barriers, tensor-map prefetch) may overlap the tail of the
@@ -399,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp <= 2) {
     // ------------------------------------------------------- MMA issuers --
-    // warp 1 takes the k-blocks with even global index, warp 2 the odd ones
+    // warp 1 takes the k-blocks with even global index, warp 2 the odd ones;
+    // k-block it uses TMEM buffer it % BUFS (BUFS is even, so each buffer has
+    // one issuer)
     const uint32_t parity = (uint32_t)(warp - 1);
     if (lane == 0) {
       uint32_t it = 0;        // global k-block index (all tiles of this CTA)
@@ -410,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((it & 1u) != parity) continue;
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
-          const int buf = (int)parity;
-          const uint32_t u = it >> 1;           // use count of this buffer
+          const int buf = (int)(it % BUFS);
+          const uint32_t u = it / BUFS;         // use count of this buffer
           if (!mbar_wait(smem_u32(&st->tempty[buf]), (u & 1u) ^ 1u, abort_flag, g.status, 2) ||
               !mbar_wait(smem_u32(&st->full[s]), ph, abort_flag, g.status, 3)) {
             alive = false;
@@ -450,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = tl.m0 + q * 32 + lane;
       const bool row_ok = row < tl.row_end;
       // weight block of this column half (both halves of a 128-wide tile share one)
-      const int nbi = tl.n0 / 128 + (kSplit ? 0 : h);
+      const int nbi = (tl.n0 + h * kAcc) / 128;
       const float* swp = g.sw + ((int64_t)tl.e * g.NB + nbi) * KB;
       const bool nb_ok = nbi < g.NB;
       float acc[kAcc];
@@ -461,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sa_next = row_ok ? __ldg(g.sa + (int64_t)kb_lo * g.M + row) : 0.0f;
       float sw_next = nb_ok ? __ldg(swp + kb_lo) : 0.0f;
       for (int kb = kb_lo; kb < kb_hi; ++kb, ++kit) {
-        const int buf = kit & 1;
-        const uint32_t u = kit >> 1;
+        const int buf = (int)(kit % BUFS);
+        const uint32_t u = kit / BUFS;
         const float f = __fmul_rn(sa_next, sw_next);
         if (kb + 1 < kb_hi) {
           sa_next = row_ok ? __ldg(g.sa + (int64_t)(kb + 1) * g.M + row) : 0.0f;
@@ -503,11 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // 32 x 64 boxes and write them with TMA tensor stores (the tensor map
           // clips columns beyond N).  The buffer was last read by the stores of
           // this warp's previous tile, a whole tile of k-blocks ago.
-          const uint32_t stg = smem_u32(ystage + (warp - 3) * kYWarpBytes);
+          const uint32_t stg = smem_u32(ystage + (warp - 3) * (F::kBoxes * kYBoxBytes));
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < F::kBoxes; ++c) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float* a8 = acc + c * 64 + j * 8;
@@ -525,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < F::kBoxes; ++c) {
               const int col0 = tl.n0 + h * kAcc + c * kYBoxCols;
               if (col0 < g.N) tma_store_2d(&tmY, stg + (uint32_t)(c * kYBoxBytes), col0, row0);
             }
@@ -535,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // ragged rows (the last m-tile, or an expert segment's end): plain stores
           __nv_bfloat16* yrow = g.y + (int64_t)row * g.ldy;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
+          for (int c = 0; c < kAcc / 8; ++c) {
             const int col = tl.n0 + h * kAcc + c * 8;
             if (col < g.N) {
               uint4 v;
@@ -553,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (!kSplit && lane == 0) bulk_wait_all();   // this warp's tensor stores are complete
+    if (F::kStaged && lane == 0) bulk_wait_all();   // this warp's tensor stores are complete
   }
 
   if (kSplit) {
@@ -591,18 +612,18 @@ fp8rl_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
                          CU_TENSOR_MAP_SWIZZLE_128B, what);
 }
 
-template <bool kGrouped, bool kSplit>
+template <bool kGrouped, int kF>
 fp8rl_status set_smem_attr(const DeviceState* ds) {
   static bool done[64] = {false};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (ds->device < 64 && done[ds->device]) return FP8RL_OK;
-  const size_t bytes = smem_bytes(kSplit);
+  const size_t bytes = smem_bytes<kF>();
   if ((size_t)ds->max_smem_optin < bytes)
     return fail(FP8RL_ERR_UNSUPPORTED_DEVICE, "GEMM needs %zu bytes of shared memory per block",
                 bytes);
   fp8rl_status st = cuda_check(
-      cudaFuncSetAttribute(gemm_w8a8_kernel<kGrouped, kSplit>,
+      cudaFuncSetAttribute(gemm_w8a8_kernel<kGrouped, kF>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes),
       "cudaFuncSetAttribute(gemm)");
   if (st == FP8RL_OK && ds->device < 64) done[ds->device] = true;
@@ -619,7 +640,7 @@ int max_active_clusters(const DeviceState* ds, int s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)s, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(true);
+  cfg.dynamicSmemBytes = smem_bytes<kSplitK>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)s;
@@ -628,7 +649,7 @@ int max_active_clusters(const DeviceState* ds, int s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_w8a8_kernel<false, true>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_w8a8_kernel<false, kSplitK>, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
     n = 0;
   }
@@ -651,28 +672,28 @@ int choose_split(const DeviceState* ds, int64_t tiles, int kb) {
 // Launches the kernel with programmatic stream serialization allowed (its
 // prologue may overlap the previous kernel; see grid_dependency_wait) and,
 // for the split-K flavour, a cluster of `cluster` CTAs along x.
-template <bool kGrouped, bool kSplit>
+template <bool kGrouped, int kF>
 fp8rl_status launch_gemm(int grid, int cluster, cudaStream_t stream, const CUtensorMap& tmA,
                          const CUtensorMap& tmB, const CUtensorMap& tmY, const GemmArgs& g,
                          const char* what) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(kSplit);
+  cfg.dynamicSmemBytes = smem_bytes<kF>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (kSplit) {
+  if (kF == kSplitK) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = (unsigned)cluster;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_w8a8_kernel<kGrouped, kSplit>, tmA, tmB, tmY, g),
+  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_w8a8_kernel<kGrouped, kF>, tmA, tmB, tmY, g),
                     what);
 }
 
@@ -709,12 +730,16 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   if (m == 0) return ok();
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FP8RL_OK) return st;
-  // Flavour: 256-wide tiles unless they would fill at most half of the SMs;
-  // then the split-K flavour with 128-wide tiles.
+  // Flavour by the number of 256-wide tiles: at least two waves of them, the
+  // wide flavour (its tile reads the fewest operand bytes per FLOP, and
+  // operand intake from L2 bounds these shapes); fewer, the narrow flavour
+  // (twice the tiles to spread, four TMEM buffers); at most half of the SMs,
+  // the split-K flavour.
   const int64_t num_m = (m + BM - 1) / BM;
-  const int64_t wide_tiles = num_m * ((n + Flavour<false>::kBN - 1) / Flavour<false>::kBN);
+  const int64_t wide_tiles = num_m * ((n + Flavour<kWide>::kBN - 1) / Flavour<kWide>::kBN);
   const bool split = wide_tiles * 2 <= ds->sm_count;
-  const int bn = split ? Flavour<true>::kBN : Flavour<false>::kBN;
+  const bool wide = !split && wide_tiles >= 2 * (int64_t)ds->sm_count;
+  const int bn = wide ? Flavour<kWide>::kBN : Flavour<kNarrow>::kBN;
   CUtensorMap tmA, tmB;
   if ((st = make_map(&tmA, qa, (uint64_t)k, (uint64_t)m, BM, "A")) != FP8RL_OK) return st;
   if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)n, (uint32_t)bn, "W")) != FP8RL_OK) return st;
@@ -738,19 +763,24 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   if (tiles > INT32_MAX) return fail(FP8RL_ERR_UNSUPPORTED_SHAPE, "too many tiles");
   if (!split) {
     g.split = 1;
-    if ((st = set_smem_attr<false, false>(ds)) != FP8RL_OK) return st;
     const int grid = (int)std::min<int64_t>(tiles, ds->sm_count);
-    st = launch_gemm<false, false>(grid, 1, stream, tmA, tmB, tmY, g, "gemm_w8a8_kernel launch");
+    if (wide) {
+      if ((st = set_smem_attr<false, kWide>(ds)) != FP8RL_OK) return st;
+      st = launch_gemm<false, kWide>(grid, 1, stream, tmA, tmB, tmY, g, "gemm_w8a8_kernel launch");
+    } else {
+      if ((st = set_smem_attr<false, kNarrow>(ds)) != FP8RL_OK) return st;
+      st = launch_gemm<false, kNarrow>(grid, 1, stream, tmA, tmB, tmY, g, "gemm_w8a8_kernel launch");
+    }
     return st == FP8RL_OK ? ok() : st;
   }
   // few tiles: exactly one cluster of g.split CTAs per tile (the kernel's
   // reduction reuses the stage buffers, so a cluster never takes a second
   // tile), split along K; a cluster of one when no larger one fits
-  if ((st = set_smem_attr<false, true>(ds)) != FP8RL_OK) return st;
+  if ((st = set_smem_attr<false, kSplitK>(ds)) != FP8RL_OK) return st;
   g.split = choose_split(ds, tiles, g.KB);
   const int clusters = (int)tiles;
-  st = launch_gemm<false, true>(clusters * g.split, g.split, stream, tmA, tmB, tmY, g,
-                                "split-K gemm_w8a8_kernel launch");
+  st = launch_gemm<false, kSplitK>(clusters * g.split, g.split, stream, tmA, tmB, tmY, g,
+                                   "split-K gemm_w8a8_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }
 
@@ -772,10 +802,10 @@ extern "C" fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, con
   if (m_total == 0) return ok();
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FP8RL_OK) return st;
-  if ((st = set_smem_attr<true, false>(ds)) != FP8RL_OK) return st;
+  if ((st = set_smem_attr<true, kWide>(ds)) != FP8RL_OK) return st;
   CUtensorMap tmA, tmB;
   if ((st = make_map(&tmA, qa, (uint64_t)k, (uint64_t)m_total, BM, "A")) != FP8RL_OK) return st;
-  if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)num_experts * n, Flavour<false>::kBN, "W")) !=
+  if ((st = make_map(&tmB, qw, (uint64_t)k, (uint64_t)num_experts * n, Flavour<kWide>::kBN, "W")) !=
       FP8RL_OK)
     return st;
   CUtensorMap tmY;
@@ -791,13 +821,13 @@ extern "C" fp8rl_status fp8rl_grouped_gemm_w8a8_blockwise(const uint8_t* qa, con
   g.KB = (int)(k / BK);
   g.NB = (int)(n / 128);
   g.num_m = 0;
-  g.num_n = (int)((n + Flavour<false>::kBN - 1) / Flavour<false>::kBN);
+  g.num_n = (int)((n + Flavour<kWide>::kBN - 1) / Flavour<kWide>::kBN);
   g.offsets = offsets;
   g.E = num_experts;
   g.status = ds->status;
   const int64_t bound = ((m_total + BM - 1) / BM + num_experts) * (int64_t)g.num_n;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(bound, ds->sm_count));
   g.split = 1;
-  st = launch_gemm<true, false>(grid, 1, stream, tmA, tmB, tmY, g, "grouped gemm_w8a8_kernel launch");
+  st = launch_gemm<true, kWide>(grid, 1, stream, tmA, tmB, tmY, g, "grouped gemm_w8a8_kernel launch");
   return st == FP8RL_OK ? ok() : st;
 }

@@ -56,6 +56,9 @@ def test_tiny_linear():
                                            (513, 1024, 2048, 0), (200, 16, 128, 0),
                                            # several tiles per CTA, ragged last n-tile
                                            (8192, 1392, 256, 8),
+                                           # narrow flavour (128-wide tiles, four TMEM
+                                           # buffers): ragged m and n tiles, padded rows
+                                           (1500, 2576, 640, 8), (1300, 4096, 2048, 0),
                                            (1000, 1280, 640, 16),
                                            # split-K flavour (128-wide tiles): S = 3 with
                                            # uneven row slices and a ragged last m-tile,
