@@ -776,8 +776,19 @@ extern "C" fp8rl_status fp8rl_gemm_w8a8_blockwise(const uint8_t* qa, const float
   // few tiles: exactly one cluster of g.split CTAs per tile (the kernel's
   // reduction reuses the stage buffers, so a cluster never takes a second
   // tile), split along K; a cluster of one when no larger one fits
+  // (the occupancy query behind choose_split needs the split flavour's
+  // shared-memory attribute set first)
   if ((st = set_smem_attr<false, kSplitK>(ds)) != FP8RL_OK) return st;
   g.split = choose_split(ds, tiles, g.KB);
+  if (g.split == 1) {
+    // no split fits: one CTA per tile, so the narrow flavour (direct output
+    // staging, four TMEM buffers) does the same work without the partial's
+    // round trip through shared memory
+    g.split = 1;
+    if ((st = set_smem_attr<false, kNarrow>(ds)) != FP8RL_OK) return st;
+    st = launch_gemm<false, kNarrow>((int)tiles, 1, stream, tmA, tmB, tmY, g, "gemm_w8a8_kernel launch");
+    return st == FP8RL_OK ? ok() : st;
+  }
   const int clusters = (int)tiles;
   st = launch_gemm<false, kSplitK>(clusters * g.split, g.split, stream, tmA, tmB, tmY, g,
                                    "split-K gemm_w8a8_kernel launch");

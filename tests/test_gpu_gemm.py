@@ -62,8 +62,9 @@ def test_tiny_linear():
                                            (1000, 1280, 640, 16),
                                            # split-K flavour (128-wide tiles): S = 3 with
                                            # uneven row slices and a ragged last m-tile,
-                                           # S = 1 (128 tiles), S = 4 with a ragged n-tile
-                                           # and padded rows, S = 2 (decode o-projection)
+                                           # no split possible (128 tiles: the narrow
+                                           # flavour, one CTA per tile), S = 4 with a ragged
+                                           # n-tile and padded rows, S = 2 (decode o)
                                            (200, 768, 384, 0), (500, 4096, 1024, 0),
                                            (100, 720, 4096, 24), (256, 4096, 1024, 0)])
 def test_shapes(m, n, k, ldy_pad):
