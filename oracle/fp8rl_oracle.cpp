@@ -149,8 +149,10 @@ float scale_from_amax(float amax) { return amax / 448.0f; }
 const uint16_t kBf16QuietNaN = 0x7FC0;
 
 // Nearest BF16 (bit pattern) to the finite float64 x, ties to even; sets
-// *hard when x is within 2^-40 (relative) of a rounding midpoint.
-uint16_t bf16_nearest(double x, bool* hard) {
+// *hard when x is within 2^-40 (relative) of a rounding midpoint.  A value
+// exactly on a midpoint with tie_dir != 0 stands for a true value just beside
+// it: tie_dir > 0 rounds to the larger magnitude, tie_dir < 0 to the smaller.
+uint16_t bf16_nearest(double x, int tie_dir, bool* hard) {
   const uint16_t sign = std::signbit(x) ? 0x8000 : 0x0000;
   const double a = std::fabs(x);
   if (a == 0.0) return sign;
@@ -162,8 +164,12 @@ uint16_t bf16_nearest(double x, bool* hard) {
   const double t = std::ldexp(a, -qe);         // exact: a in units of the spacing
   double n = std::floor(t);
   const double frac = t - n;                   // exact
-  if (std::fabs(frac - 0.5) <= std::ldexp(t, -40)) *hard = true;
-  if (frac > 0.5 || (frac == 0.5 && std::fmod(n, 2.0) != 0.0)) n += 1.0;
+  if (frac == 0.5 && tie_dir != 0) {
+    if (tie_dir > 0) n += 1.0;
+  } else {
+    if (std::fabs(frac - 0.5) <= std::ldexp(t, -40)) *hard = true;
+    if (frac > 0.5 || (frac == 0.5 && std::fmod(n, 2.0) != 0.0)) n += 1.0;
+  }
   const double v = std::ldexp(n, qe);          // a BF16 value (or 2^128)
   if (v >= std::ldexp(1.0, 128)) return sign | 0x7F80;
   const float f = (float)v;                    // exact
@@ -173,6 +179,17 @@ uint16_t bf16_nearest(double x, bool* hard) {
 }
 
 // y = BF16_RNE(silu(g) * u) for BF16 inputs (bit patterns).
+//
+// Two families of products sit exactly on a BF16 midpoint in float64 while
+// the true product does not, and their direction is known:
+//   * g > 0 with e^-g below half a float64 ulp of 1: float64 gives silu = g,
+//     while silu(g) = g - g e^-g / (1 + e^-g) is strictly smaller, so the
+//     true |x| lies just below |g u|;
+//   * |g| so small that e^-g rounds to 1: float64 gives silu = g / 2, while
+//     silu(g) = g/2 + g^2/4 - ... lies strictly above g/2, so the true x lies
+//     just beside (g/2) u, on the larger-magnitude side when g > 0 and the
+//     smaller when g < 0.
+// Any other product closer than 2^-40 to a midpoint is flagged.
 uint16_t silu_mul_bf16_one(uint16_t gb, uint16_t ub, bool* hard) {
   const double g = bf16_to_float(gb), u = bf16_to_float(ub);
   if (std::isnan(g) || std::isnan(u)) return kBf16QuietNaN;
@@ -186,15 +203,20 @@ uint16_t silu_mul_bf16_one(uint16_t gb, uint16_t ub, bool* hard) {
   if (std::isinf(u)) return (uint16_t)(sx | 0x7F80);
   if (u == 0.0) return sx;
   double s;
+  int tie_dir = 0;
   if (g > 0) {
-    s = g / (1.0 + std::exp(-g));
+    const double e = std::exp(-g);
+    s = g / (1.0 + e);
+    if (1.0 + e == 1.0) tie_dir = -1;          // float64 silu = g; true silu < g
+    else if (e == 1.0) tie_dir = +1;           // float64 silu = g/2; true silu > g/2
   } else {
     const double e = std::exp(g);              // 0 below about -745: |y| rounds to 0 there
     s = g * e / (1.0 + e);
+    if (e == 1.0) tie_dir = -1;                // float64 silu = g/2; true |silu| < |g|/2
   }
   const double x = s * u;
   if (x == 0.0) return sx;                     // |x| < 2^-900: far below the smallest BF16
-  return bf16_nearest(x, hard);
+  return bf16_nearest(x, tie_dir, hard);
 }
 
 // binary32 -> BF16, round to nearest even (NaN stays a quiet NaN).

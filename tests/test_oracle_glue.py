@@ -131,6 +131,19 @@ def test_silu_mul_large_gate_closed_form():
     assert (y[~fin] == 0x7F80).all()                              # beyond BF16 max: +inf
 
 
+def test_silu_mul_structural_midpoints_match_decimal():
+    """The oracle settles exact float64 midpoints of large and tiny gates by the
+    sign of silu's remainder; an 80-digit decimal evaluation agrees on a sample."""
+    rng = np.random.default_rng(44)
+    big = rng.integers(0x4240, 0x7F80, size=300)                 # g in [48, max]
+    tiny = rng.integers(1, 0x1B00, size=300) | rng.integers(0, 2, size=300) * 0x8000
+    for gb in np.concatenate([big, tiny]).astype(np.uint16):
+        for ub in (0x3FC0, 0xBFA0, 0x4330, 0x3F81):
+            y = int(oracle.silu_mul_pairs(np.array([gb]), np.array([ub], np.uint16))[0])
+            d = oracle.silu_mul_decimal(int(gb), ub, y)
+            assert y == d, (hex(gb), hex(ub), hex(y), hex(d))
+
+
 def test_silu_mul_special_values():
     P0, N0, PI, NI, NAN = 0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC0
     one, m_one, big_neg = 0x3F80, 0xBF80, 0xC400                  # 1, -1, -512
