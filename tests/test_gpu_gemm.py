@@ -54,8 +54,11 @@ def test_tiny_linear():
 @pytest.mark.parametrize("m,n,k,ldy_pad", [(1, 256, 128, 0), (127, 512, 1024, 8), (129, 272, 256, 0),
                                            (300, 512, 384, 40), (64, 256, 512, 0),
                                            (513, 1024, 2048, 0), (200, 16, 128, 0),
-                                           # several tiles per CTA, ragged last n-tile
-                                           (8192, 1392, 256, 8),
+                                           # wide flavour (128 x 256 tiles), several tiles
+                                           # per CTA, ragged last n-tile; ragged last m-tile
+                                           # (100 and 72 rows)
+                                           (8192, 1392, 256, 8), (8292, 1392, 256, 0),
+                                           (8264, 1280, 384, 16),
                                            # narrow flavour (128-wide tiles, four TMEM
                                            # buffers): ragged m and n tiles, padded rows
                                            (1500, 2576, 640, 8), (1300, 4096, 2048, 0),
