@@ -12,7 +12,7 @@
 // The scales are arbitrary binary32 numbers (amax/448), so they cannot ride on
 // the hardware's block-scaled MMA (power-of-two UE8M0 scales per 32 K).  Each
 // 128-wide k-block is therefore one MMA group writing a fresh FP32 partial
-// P_kb into tensor memory; epilogue warps read it back (tcgen05.ld, 32 columns per wait), multiply
+// P_kb into tensor memory; epilogue warps read it back (tcgen05.ld, 16 columns at a time), multiply
 // by sa*sw and add it into FP32 register accumulators (packed FP32x2 FMAs;
 // the scales of k-block kb+1 are fetched while kb is promoted).
 //
@@ -494,23 +494,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!okw) { alive = false; break; }
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * kBN + h * kAcc);
-        // 32 columns per round trip: two loads in flight, then one wait
-        uint32_t p[32];
-        uint32_t (&p0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&p[0]);
-        uint32_t (&p1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&p[16]);
+        uint32_t p[16];
 #pragma unroll
-        for (int c = 0; c < kAcc / 32; ++c) {
-          tmem_ld16(taddr + c * 32, p0);
-          tmem_ld16(taddr + c * 32 + 16, p1);
+        for (int c = 0; c < kAcc / 16; ++c) {
+          tmem_ld16(taddr + c * 16, p);
           tmem_wait_ld();
-          if (c == kAcc / 32 - 1) {
+          if (c == kAcc / 16 - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&st->tempty[buf]));
           }
 #pragma unroll
-          for (int j = 0; j < 32; j += 2)
-            ffma2(acc[c * 32 + j], acc[c * 32 + j + 1], p[j], p[j + 1], f);
+          for (int j = 0; j < 16; j += 2)
+            ffma2(acc[c * 16 + j], acc[c * 16 + j + 1], p[j], p[j + 1], f);
         }
       }
       if (!alive) break;
