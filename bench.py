@@ -524,8 +524,8 @@ def _timed(fn):
 def _cpu_baseline_rows(W):
     """The oracle timed on every row of the step, on the host cores, with inputs
     of the same recipes generated on the host.  Full workloads where the
-    oracle finishes in about a second (activation quantization, MoE glue,
-    TIS, MIS); otherwise a sample, scaled to the row's full workload by its
+    oracle finishes in about a second (activation quantization, the M = 256
+    GEMMs, MoE glue, TIS, MIS); otherwise a sample, scaled to the row's full workload by its
     work (elements, rows or sequences) and marked "extrapolated".  Returns
     {row: {"cpu_ms": ms for the row's full workload, "sample": ...,
     "extrapolated": bool}}."""
@@ -553,6 +553,12 @@ def _cpu_baseline_rows(W):
         m, n, k = g["m"], g["n"], g["k"]
         a = wl.dense_acts(m, k, seed=wl.sub_seed(3, m, n, k))
         tq, (qa, sa) = _timed(lambda: oracle.quantize_act_groupwise(a))
+        if m <= 256:
+            # decode-sized: the whole GEMM (about a second of host time per shape)
+            tg, _ = _timed(lambda: oracle.gemm_w8a8(qa, sa, wq[g["name"]][0], wq[g["name"]][1]))
+            out[key] = {"act_quant_cpu_ms": tq, "gemm_cpu_ms": tg, "extrapolated": False,
+                        "sample": "full: act-quant [%d, %d], GEMM [%d, %d, %d]" % (m, k, m, n, k)}
+            continue
         rows = (np.arange(nr) * (m // nr)).astype(np.int64)
         tg, _ = _timed(lambda: oracle.gemm_w8a8(qa, sa, wq[g["name"]][0], wq[g["name"]][1], rows=rows))
         out[key] = {"act_quant_cpu_ms": tq, "gemm_cpu_ms": tg * m / nr, "extrapolated": True,
