@@ -12,11 +12,11 @@
 // fill the GPU; up to 8 for small batches), rank r taking a contiguous range
 // of the sequence's 64-token stages.  In each CTA a producer warp TMA-loads the head's
 // 128-byte slice of 64 consecutive tokens of K and of V per stage (16 KB, in
-// the 128-byte swizzled layout when the boxes allow it) into a 6-slot
+// the 128-byte swizzled layout when the boxes allow it) into a 3-slot
 // mbarrier ring, with the stage's valid-token mask; its lanes look up the
 // pages of a stage's boxes together, one stage ahead.  Three consumer warps
 // take whole stages in turn, warp w the stages i with i % 3 == w, so that a
-// slot (i % 6) always has the same consumer, which waits on its barrier in
+// slot (i % 3) always has the same consumer, which waits on its barrier in
 // order (a warp can never wait on a slot whose previous phase another warp
 // has not consumed yet).  Both contractions of a stage run on the tensor cores as
 // m16n8k16 FP16 MMAs with FP32 accumulation, the G <= 8 query heads of the
@@ -56,7 +56,12 @@ constexpr int kConsumerWarps = 3;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;          // + producer warp
 constexpr int kStageTokens = 64;
 constexpr int kMTiles = kStageTokens / 16;                       // 16-token MMA tiles per stage
-constexpr int kStages = 6;
+// Three slots of 16 KB (one per consumer warp) and at most 128 registers a
+// thread let four CTAs share an SM: 608 resident CTAs, so the 512 (sequence,
+// head) pairs of a 64-sequence, 8-head batch run in one wave instead of 1.7
+// waves of 304 (the second one too thin to keep HBM busy).  Bytes in flight
+// per SM stay the same (4 x 48 KB against 2 x 96 KB).
+constexpr int kStages = 3;
 constexpr int kHalfStage = kStageTokens * kHeadDim;              // K (or V) of a stage: 8 KB
 constexpr int kStageBytes = 2 * kHalfStage;
 constexpr int kMaxG = 8;                                         // the MMA's n
@@ -158,7 +163,7 @@ __device__ __forceinline__ int token_row(const AttnParams& p, int s, int t, int 
 // kSwz: the stage rows are in the 128-byte swizzled layout (16-byte chunk j
 // of row r stored at chunk j ^ (r % 8)); otherwise plain 128-byte rows.
 template <bool kSwz>
-__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(
+__global__ void __launch_bounds__(kAttnThreads, 4) attn_decode_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
