@@ -633,8 +633,9 @@ def _cores():
 
 
 def _link_rates(dev, nbytes: int = 1 << 31):
-    """This box's pinned host<->device copy rates (GB/s, best of 3): one
-    direction at a time, and both at once on two streams."""
+    """This box's pinned host<->device copy rates (GB/s, best of 3, with the
+    median beside them): one direction at a time, and both at once on two
+    streams."""
     import torch
     host_a = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     host_b = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
@@ -642,7 +643,9 @@ def _link_rates(dev, nbytes: int = 1 << 31):
     dev_b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def best(fn):
+    trials = {}
+
+    def best(fn, key):
         out = []
         for _ in range(3):
             torch.cuda.synchronize()
@@ -650,6 +653,7 @@ def _link_rates(dev, nbytes: int = 1 << 31):
             fn()
             torch.cuda.synchronize()
             out.append(time.perf_counter() - t0)
+        trials[key] = sorted(out)
         return min(out)
 
     def both():
@@ -658,11 +662,14 @@ def _link_rates(dev, nbytes: int = 1 << 31):
         with torch.cuda.stream(s2):
             host_b.copy_(dev_b, non_blocking=True)
 
-    h2d = nbytes / best(lambda: dev_a.copy_(host_a, non_blocking=True)) / 1e9
-    d2h = nbytes / best(lambda: host_b.copy_(dev_b, non_blocking=True)) / 1e9
-    bi = 2 * nbytes / best(both) / 1e9
+    h2d = nbytes / best(lambda: dev_a.copy_(host_a, non_blocking=True), "h2d") / 1e9
+    d2h = nbytes / best(lambda: host_b.copy_(dev_b, non_blocking=True), "d2h") / 1e9
+    bi = 2 * nbytes / best(both, "bi") / 1e9
     del host_a, host_b, dev_a, dev_b
-    return {"h2d_gbs": h2d, "d2h_gbs": d2h, "bidirectional_gbs": bi, "buffer_bytes": nbytes}
+    return {"h2d_gbs": h2d, "d2h_gbs": d2h, "bidirectional_gbs": bi, "buffer_bytes": nbytes,
+            "median_gbs": {"h2d": nbytes / trials["h2d"][1] / 1e9,
+                           "d2h": nbytes / trials["d2h"][1] / 1e9,
+                           "bidirectional": 2 * nbytes / trials["bi"][1] / 1e9}}
 
 
 def run_reference(args):
@@ -785,18 +792,24 @@ def run_ours(args):
         e2e_step()
         torch.cuda.synchronize()
         e_steps = max(1, min(args.steps, 3))
-        barrier()
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record()
-        for _ in range(e_steps):
-            e2e_step()
-        s1.record()
-        barrier()
-        e_ms = s0.elapsed_time(s1)
-        e_ms = max_over_ranks([e_ms], dev, world)[0]
-        e2e = {"value": replica_gbs(world, W.req_bytes, e_steps, e_ms), "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
+        # several timed windows of e_steps steps each: the host link is shared
+        # with the rest of the machine, and its rate can change from one window
+        # to the next; the value is the median window, the others are listed
+        windows = []
+        for _ in range(5):
+            barrier()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record()
+            for _ in range(e_steps):
+                e2e_step()
+            s1.record()
+            barrier()
+            e_ms = max_over_ranks([s0.elapsed_time(s1)], dev, world)[0]
+            windows.append(replica_gbs(world, W.req_bytes, e_steps, e_ms))
+        e2e = {"value": statistics.median(windows), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "windows": len(windows), "windows_gbs": windows, "best_gbs": max(windows)}
         del hw, hq, hs, work
         # the host link's own bound for this step's copies
         link = _link_rates(dev)
