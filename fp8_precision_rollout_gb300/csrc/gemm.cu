@@ -35,13 +35,17 @@
 //               written by TMA tensor stores (plain stores for ragged rows).
 //   TMEM: two partial buffers as wide as the tile (all 512 columns for the
 //   256-wide tile), so the MMA of k-block kb+1 overlaps the promotion of kb.
-// Decode-sized problems (fewer 256-wide output tiles than half the SMs) run
-// the split-K flavour: 128-wide tiles, so that twice as many CTAs share the
-// work and each k-block's MMA and promotion take half as long, and a cluster
-// of 1-4 CTAs per tile, each over a slice of the k-blocks.  Each CTA stages its FP32 partial tile in its own (by then idle)
-// pipeline buffers; rank r then reads rows [r*128/S, (r+1)*128/S) of all S
-// partials through distributed shared memory, sums them in rank order and
-// stores them (reduce-scatter, no global scratch, deterministic).
+// Mid-sized problems (fewer than two waves of 256-wide tiles) run the narrow
+// flavour: 128 x 128 tiles and four TMEM partial buffers.  Decode-sized
+// problems (256-wide tiles for at most half the SMs) run the split-K flavour:
+// 128-wide tiles, so that twice as many CTAs share the work and each
+// k-block's MMA and promotion take half as long, and a cluster of 2-4 CTAs
+// per tile, each over a slice of the k-blocks (the narrow flavour, one CTA
+// per tile, when no cluster of two fits).  Each split CTA stages its FP32
+// partial tile in its own (by then idle) pipeline buffers; rank r then reads
+// rows [r*128/S, (r+1)*128/S) of all S partials through distributed shared
+// memory, sums them in rank order and stores them (reduce-scatter, no global
+// scratch, deterministic).
 // Every wait on an mbarrier is bounded (1 s); on expiry the kernel records it
 // in the library's device status word, drains what it issued and returns.
 #include <cuda_bf16.h>
